@@ -1,0 +1,225 @@
+"""CPU oracle for the FP4 (E2M1) block-scaled decode path -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference arm may import this package. The GPU library never calls it and shares
+no code with it: the arithmetic lives in ``fp4_oracle.c`` (plain C, one element
+at a time, fp32 where the pages fix fp32), and this module only compiles that
+file with gcc and marshals numpy arrays through ctypes.
+
+Functions and the passages they follow (web pages cited by title and section):
+
+* ``mx_unpack`` / ``mx_unpack_old_sequence`` / ``mx_unpack_at`` -- MXFP4 unpack,
+  "vllm-project/vllm pull 51583" (prhub digest), "Motivation" and
+  "Implementation breakdown" items 1-2: E2M1 code -> bf16 bits, E8M0 scale as a
+  wrapping int16 add of (E-127)<<7, zero codes forced to +0.0 lane by lane.
+* ``e4m3_to_f32``, ``f32_to_bf16_rne``, ``e2m1_bf16_bits`` -- the element
+  conversions those steps use (OCP FP8 E4M3 definition; IEEE round to nearest
+  even into bf16; the E2M1 codebook).
+* ``nv_embedding_gather`` / ``nv_embedding_gather_at`` -- NVFP4 gather-dequant,
+  "sgl-project/sglang pull 34222" (prhub digest), "Implementation breakdown"
+  item 2 and the ``reference_dequant`` test oracle: value * (e4m3 block scale *
+  fp32 global scale) in fp32, rounded to bf16.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` to values the pages
+print, closed forms and library routines; ``tests/test_oracle_mutants.py`` checks
+that plausible mistakes planted in a copy of the C source fail those pins.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "fp4_oracle.c")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIBRARY = os.path.join(BUILD_DIR, "libfp4oracle.so")
+
+_BASE_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_source(source: str, output: str, openmp: bool = True) -> str:
+    """Compile an oracle C source into a shared library with gcc.
+
+    Tries OpenMP first (for the timed multi-core baseline) and falls back to a
+    single-threaded build when the compiler or runtime lacks it.
+    """
+    os.makedirs(os.path.dirname(output), exist_ok=True)
+    tmp = f"{output}.{os.getpid()}.tmp"
+    attempts = ([["-fopenmp"]] if openmp else []) + [[]]
+    last = None
+    for extra in attempts:
+        cmd = ["gcc", *_BASE_FLAGS, *extra, source, "-o", tmp, "-lm"]
+        proc = subprocess.run(cmd, capture_output=True, text=True)
+        if proc.returncode == 0:
+            os.replace(tmp, output)
+            return output
+        last = proc
+    raise RuntimeError(f"oracle build failed:\n{last.stderr if last else ''}")
+
+
+def build(force: bool = False) -> str:
+    """Build ``_build/libfp4oracle.so`` if missing or older than its source."""
+    with _lock:
+        stale = (not os.path.exists(LIBRARY)
+                 or os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE))
+        if force or stale:
+            compile_source(SOURCE, LIBRARY)
+    return LIBRARY
+
+
+_P8 = ctypes.POINTER(ctypes.c_uint8)
+_P16 = ctypes.POINTER(ctypes.c_uint16)
+_P64 = ctypes.POINTER(ctypes.c_int64)
+
+
+def bind(path: str):
+    """Load an oracle library and declare its signatures."""
+    lib = ctypes.CDLL(path)
+    lib.oracle_e2m1_bf16_bits.argtypes = [ctypes.c_uint]
+    lib.oracle_e2m1_bf16_bits.restype = ctypes.c_uint16
+    lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_bf16_rne.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16_rne.restype = ctypes.c_uint16
+    for name in ("oracle_mx_unpack", "oracle_mx_unpack_old_sequence"):
+        fn = getattr(lib, name)
+        fn.argtypes = [_P8, _P8, ctypes.c_int64, _P16, ctypes.c_int]
+        fn.restype = None
+    lib.oracle_mx_unpack_at.argtypes = [_P8, _P8, _P64, ctypes.c_int64, _P16]
+    lib.oracle_mx_unpack_at.restype = None
+    lib.oracle_nv_embedding_gather.argtypes = [
+        _P64, ctypes.c_int64, _P8, _P8, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, _P16, ctypes.c_int]
+    lib.oracle_nv_embedding_gather.restype = ctypes.c_int64
+    lib.oracle_nv_embedding_gather_at.argtypes = [
+        _P64, _P8, _P8, ctypes.c_float, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        _P64, _P64, ctypes.c_int64, _P16]
+    lib.oracle_nv_embedding_gather_at.restype = None
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = bind(build())
+    return _lib
+
+
+def _u8(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError(f"expected uint8, got {a.dtype}")
+    return a
+
+
+def _i64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class Oracle:
+    """numpy-facing wrapper over one loaded oracle library (the real one, or a
+    test-built variant)."""
+
+    def __init__(self, library):
+        self.lib = library
+
+    # -- element conversions ------------------------------------------------
+    def e2m1_bf16_bits(self, code: int) -> int:
+        return int(self.lib.oracle_e2m1_bf16_bits(code))
+
+    def e4m3_to_f32(self, byte: int) -> float:
+        return float(self.lib.oracle_e4m3_to_f32(byte))
+
+    def f32_to_bf16_rne(self, value) -> int:
+        return int(self.lib.oracle_f32_to_bf16_rne(float(np.float32(value))))
+
+    # -- MXFP4 ----------------------------------------------------------------
+    def _mx(self, fn, packed, scales, threads):
+        packed, scales = _u8(packed).reshape(-1), _u8(scales).reshape(-1)
+        n = packed.size * 2
+        if n % 32 or scales.size != n // 32:
+            raise ValueError("need packed[n/2] and scales[n/32] with n % 32 == 0")
+        out = np.empty(n, dtype=np.uint16)
+        fn(_ptr(packed, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8), n,
+           _ptr(out, ctypes.c_uint16), int(threads))
+        return out
+
+    def mx_unpack(self, packed, scales, threads: int = 1) -> np.ndarray:
+        """Flat bf16 bits (uint16[n]) of a packed stream."""
+        return self._mx(self.lib.oracle_mx_unpack, packed, scales, threads)
+
+    def mx_unpack_old_sequence(self, packed, scales, threads: int = 1) -> np.ndarray:
+        return self._mx(self.lib.oracle_mx_unpack_old_sequence, packed, scales, threads)
+
+    def mx_unpack_at(self, packed, scales, idx) -> np.ndarray:
+        packed, scales, idx = _u8(packed).reshape(-1), _u8(scales).reshape(-1), _i64(idx)
+        n = packed.size * 2
+        if idx.size and (idx.min() < 0 or idx.max() >= n):
+            raise IndexError("element index out of range")
+        out = np.empty(idx.size, dtype=np.uint16)
+        self.lib.oracle_mx_unpack_at(_ptr(packed, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                     _ptr(idx, ctypes.c_int64), idx.size,
+                                     _ptr(out, ctypes.c_uint16))
+        return out
+
+    # -- NVFP4 ----------------------------------------------------------------
+    def nv_embedding_gather(self, ids, weight, scales, global_scale, group_size: int = 16,
+                            threads: int = 1):
+        """Returns (uint16[*ids.shape, hidden], number of out-of-range ids)."""
+        ids_shape = np.shape(ids)
+        ids = _i64(ids).reshape(-1)
+        weight, scales = _u8(weight), _u8(scales)
+        vocab, half = weight.shape
+        hidden = 2 * half
+        if scales.shape != (vocab, hidden // group_size):
+            raise ValueError("scales must be [vocab, hidden / group_size]")
+        out = np.empty((ids.size, hidden), dtype=np.uint16)
+        bad = self.lib.oracle_nv_embedding_gather(
+            _ptr(ids, ctypes.c_int64), ids.size, _ptr(weight, ctypes.c_uint8),
+            _ptr(scales, ctypes.c_uint8), float(np.float32(global_scale)), vocab, hidden,
+            group_size, _ptr(out, ctypes.c_uint16), int(threads))
+        return out.reshape(*ids_shape, hidden), int(bad)
+
+    def nv_embedding_gather_at(self, ids, weight, scales, global_scale, rows, cols,
+                               group_size: int = 16) -> np.ndarray:
+        ids = _i64(ids).reshape(-1)
+        weight, scales = _u8(weight), _u8(scales)
+        rows, cols = _i64(rows), _i64(cols)
+        vocab, half = weight.shape
+        hidden = 2 * half
+        if rows.size and (rows.min() < 0 or rows.max() >= ids.size
+                          or cols.min() < 0 or cols.max() >= hidden):
+            raise IndexError("sample index out of range")
+        out = np.empty(rows.size, dtype=np.uint16)
+        self.lib.oracle_nv_embedding_gather_at(
+            _ptr(ids, ctypes.c_int64), _ptr(weight, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+            float(np.float32(global_scale)), vocab, hidden, group_size,
+            _ptr(rows, ctypes.c_int64), _ptr(cols, ctypes.c_int64), rows.size,
+            _ptr(out, ctypes.c_uint16))
+        return out
+
+    def max_threads(self) -> int:
+        return int(self.lib.oracle_max_threads())
+
+
+_default = None
+
+
+def get() -> Oracle:
+    """The oracle built from ``fp4_oracle.c``."""
+    global _default
+    if _default is None:
+        _default = Oracle(lib())
+    return _default
