@@ -1,0 +1,142 @@
+"""GB300 (sm_103a) decode of block-scaled FP4 (E2M1) into bf16.
+
+Python binding of the C ABI in ``include/fp4mx.h``. The functions below carry the
+C entry points' names and only marshal arguments: they check dtypes, devices and
+shapes, allocate the output tensor when none is given, and pass raw device
+pointers plus the current CUDA stream to the library, where every step of the
+decode runs in hand-written CUDA kernels. PyTorch supplies device memory and
+streams only. There is no CPU path: CPU tensors, a missing library or a non-OK
+status raise.
+
+* ``fp4_mx_unpack(packed, scales_e8m0)`` -- MXFP4: E8M0 scale per 32 codes,
+  applied as a wrapping int16 add of (E-127)<<7 into the bf16 exponent field,
+  zero codes forced to +0.0 ("vllm-project/vllm pull 51583", "Motivation",
+  "Implementation breakdown").
+* ``fp4_nv_embedding_gather(ids, weight, block_scale, global_scale)`` -- NVFP4
+  embedding lookup dequantised at gather time: value * (e4m3 block scale * fp32
+  global scale) in fp32, rounded to bf16 ("sgl-project/sglang pull 34222",
+  "Implementation breakdown", "Key source snippets").
+"""
+from __future__ import annotations
+
+from ._lib import Status, last_error, library_path, load, status_string  # noqa: F401
+
+__all__ = ["fp4_mx_unpack", "fp4_nv_embedding_gather", "fp4_status_string", "Fp4Error",
+           "Status", "load", "library_path"]
+
+
+class Fp4Error(ValueError):
+    """A non-OK status from the library."""
+
+    def __init__(self, where: str, code: int):
+        self.code = Status(code) if code in Status._value2member_map_ else code
+        detail = last_error() if code == Status.ERR_CUDA or code == Status.ERR_POINTER else ""
+        super().__init__(f"{where}: {status_string(code)}" + (f" ({detail})" if detail else ""))
+
+
+def fp4_status_string(code: int) -> str:
+    return status_string(code)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check_cuda(t, name: str, dtypes):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path), got {t.device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes_void(stream.cuda_stream)
+
+
+def ctypes_void(v):
+    import ctypes
+    return ctypes.c_void_p(int(v) if v else None)
+
+
+def _ptr(t):
+    return ctypes_void(t.data_ptr()) if t is not None and t.numel() else ctypes_void(0)
+
+
+def fp4_mx_unpack(packed, scales_e8m0, out=None, stream=None):
+    """MXFP4 -> bf16. ``packed`` uint8 [..., k/2], ``scales_e8m0`` uint8 [..., k/32]
+    with the same leading dimensions; returns (or fills ``out``) bf16 [..., k].
+    Enqueued on ``stream`` (default: the current stream of the tensors' device)."""
+    torch = _torch()
+    _check_cuda(packed, "packed", (torch.uint8,))
+    _check_cuda(scales_e8m0, "scales_e8m0", (torch.uint8,))
+    if packed.dim() < 1 or scales_e8m0.dim() != packed.dim():
+        raise ValueError("packed and scales_e8m0 must have the same number of dimensions")
+    if packed.shape[:-1] != scales_e8m0.shape[:-1]:
+        raise ValueError("packed and scales_e8m0 leading dimensions differ")
+    k = packed.shape[-1] * 2
+    if scales_e8m0.shape[-1] * 32 != k:
+        raise ValueError(f"scales_e8m0 last dim must be k/32 = {k // 32}")
+    rows = packed.numel() // packed.shape[-1] if packed.shape[-1] else 0
+    shape = (*packed.shape[:-1], k)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=packed.device)
+    else:
+        _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
+        if tuple(out.shape) != shape:
+            raise ValueError(f"out must have shape {shape}")
+    code = load().fp4_mx_unpack(_ptr(packed), _ptr(scales_e8m0), _ptr(out), rows, k,
+                                _stream_handle(stream, packed.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_mx_unpack", code)
+    return out
+
+
+def fp4_nv_embedding_gather(ids, weight, block_scale, global_scale, group_size: int = 16,
+                            out=None, err_flag=None, stream=None):
+    """NVFP4 embedding gather-dequant -> bf16 [*ids.shape, hidden].
+
+    ``ids`` int64 (any shape), ``weight`` uint8 [vocab, hidden/2], ``block_scale``
+    float8_e4m3fn (or its uint8 bits) [vocab, hidden/16], ``global_scale`` fp32
+    CUDA tensor with one element. ``err_flag`` (optional int32 CUDA tensor with one
+    element) is set to Status.ERR_INDEX when an id is outside [0, vocab); such a
+    row is written as +0.0."""
+    torch = _torch()
+    _check_cuda(ids, "ids", (torch.int64,))
+    _check_cuda(weight, "weight", (torch.uint8,))
+    _check_cuda(block_scale, "block_scale", (torch.float8_e4m3fn, torch.uint8))
+    _check_cuda(global_scale, "global_scale", (torch.float32,))
+    if global_scale.numel() != 1:
+        raise ValueError("global_scale must have exactly one element")
+    if weight.dim() != 2 or block_scale.dim() != 2:
+        raise ValueError("weight and block_scale must be 2-D [vocab, ...]")
+    vocab, half = weight.shape
+    hidden = 2 * half
+    if block_scale.shape[0] != vocab:
+        raise ValueError("weight and block_scale have different vocab sizes")
+    if group_size > 0 and hidden % group_size == 0 and block_scale.shape[1] * group_size != hidden:
+        raise ValueError(f"block_scale must be [vocab, hidden/{group_size}]")
+    shape = (*ids.shape, hidden)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=weight.device)
+    else:
+        _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
+        if tuple(out.shape) != shape:
+            raise ValueError(f"out must have shape {shape}")
+    if err_flag is not None:
+        _check_cuda(err_flag, "err_flag", (torch.int32,))
+    code = load().fp4_nv_embedding_gather(
+        _ptr(ids), ids.numel(), _ptr(weight), _ptr(block_scale), _ptr(global_scale), vocab,
+        hidden, int(group_size), _ptr(out), _ptr(err_flag),
+        _stream_handle(stream, weight.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_nv_embedding_gather", code)
+    return out

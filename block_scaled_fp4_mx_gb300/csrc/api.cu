@@ -1,0 +1,181 @@
+// api.cu -- the exported C ABI (include/fp4mx.h): host-side argument checks,
+// then one kernel launch on the caller's stream. No allocation, no
+// synchronisation, no host<->device copies.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "fp4mx.h"
+#include "launch.h"
+
+#define FP4_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+void clear_error() { g_last_error[0] = '\0'; }
+
+fp4_status cuda_failure(cudaError_t err, const char *where) {
+    std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where,
+                  cudaGetErrorString(err), cudaGetErrorName(err));
+    return FP4_ERR_CUDA;
+}
+
+bool overlaps(const void *a, uint64_t a_bytes, const void *b, uint64_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+// The pointer must be memory the current device can address: device or
+// managed memory of this device, or mapped pinned host memory.
+fp4_status check_device_pointer(const void *p, int device) {
+    cudaPointerAttributes attr;
+    const cudaError_t err = cudaPointerGetAttributes(&attr, p);
+    if (err != cudaSuccess) return cuda_failure(err, "cudaPointerGetAttributes");
+    switch (attr.type) {
+    case cudaMemoryTypeDevice:
+        if (attr.device != device) {
+            std::snprintf(g_last_error, sizeof g_last_error,
+                          "pointer %p belongs to device %d, current device is %d", p,
+                          attr.device, device);
+            return FP4_ERR_POINTER;
+        }
+        return FP4_OK;
+    case cudaMemoryTypeManaged:
+        return FP4_OK;
+    case cudaMemoryTypeHost:
+        if (attr.devicePointer == p) return FP4_OK;
+        break;
+    default:
+        break;
+    }
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "pointer %p is not device-accessible CUDA memory", p);
+    return FP4_ERR_POINTER;
+}
+
+fp4_status check_pointers(const void *const *ptrs, int n) {
+    int device = 0;
+    const cudaError_t err = cudaGetDevice(&device);
+    if (err != cudaSuccess) return cuda_failure(err, "cudaGetDevice");
+    for (int i = 0; i < n; ++i) {
+        if (ptrs[i] == nullptr) continue;
+        const fp4_status s = check_device_pointer(ptrs[i], device);
+        if (s != FP4_OK) return s;
+    }
+    return FP4_OK;
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kSlots = 8;
+std::atomic<int> g_resident[kMaxDevices][kSlots];
+
+}  // namespace
+
+namespace fp4mx {
+
+int max_resident_ctas(const void *kernel, int threads, int slot) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+        return 1024;
+    int cached = g_resident[device][slot].load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) !=
+            cudaSuccess ||
+        sms <= 0 || per_sm <= 0) {
+        cudaGetLastError();
+        return 1024;
+    }
+    cached = sms * per_sm;
+    g_resident[device][slot].store(cached, std::memory_order_relaxed);
+    return cached;
+}
+
+}  // namespace fp4mx
+
+FP4_EXPORT fp4_status fp4_mx_unpack(const uint8_t *packed, const uint8_t *scales_e8m0,
+                                    uint16_t *out_bf16, int64_t rows, int64_t k,
+                                    fp4_stream_t stream) {
+    clear_error();
+    if (rows < 0 || k < 0 || k % 32 != 0) return FP4_ERR_SHAPE;
+    if (rows == 0 || k == 0) return FP4_OK;
+    if (rows > INT64_MAX / 2 / k) return FP4_ERR_SHAPE;  // rows * k * 2 bytes must fit
+    if (packed == nullptr || scales_e8m0 == nullptr || out_bf16 == nullptr)
+        return FP4_ERR_NULL_PTR;
+    const int64_t n = rows * k;
+    const uint64_t out_bytes = (uint64_t)n * 2;
+    if (overlaps(out_bf16, out_bytes, packed, (uint64_t)n / 2) ||
+        overlaps(out_bf16, out_bytes, scales_e8m0, (uint64_t)n / 32))
+        return FP4_ERR_ALIAS;
+    const void *ptrs[] = {packed, scales_e8m0, out_bf16};
+    const fp4_status s = check_pointers(ptrs, 3);
+    if (s != FP4_OK) return s;
+    const cudaError_t err =
+        fp4mx::launch_mx_unpack(packed, scales_e8m0, out_bf16, n, (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_unpack launch");
+}
+
+FP4_EXPORT fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_ids,
+                                              const uint8_t *weight,
+                                              const uint8_t *block_scale_e4m3,
+                                              const float *global_scale, int64_t vocab,
+                                              int64_t hidden, int64_t group_size,
+                                              uint16_t *out_bf16, int32_t *err_flag,
+                                              fp4_stream_t stream) {
+    clear_error();
+    if (num_ids < 0 || vocab < 0 || hidden <= 0 || group_size <= 0) return FP4_ERR_SHAPE;
+    if (hidden % group_size != 0) return FP4_ERR_GROUP;
+    if (group_size != 16) return FP4_ERR_UNSUPPORTED;
+    if (num_ids == 0) return FP4_OK;
+    if (vocab == 0) return FP4_ERR_SHAPE;
+    if (num_ids > INT64_MAX / 2 / hidden || vocab > INT64_MAX / hidden) return FP4_ERR_SHAPE;
+    if (ids == nullptr || weight == nullptr || block_scale_e4m3 == nullptr ||
+        global_scale == nullptr || out_bf16 == nullptr)
+        return FP4_ERR_NULL_PTR;
+    const uint64_t out_bytes = (uint64_t)num_ids * (uint64_t)hidden * 2;
+    const uint64_t w_bytes = (uint64_t)vocab * (uint64_t)hidden / 2;
+    const uint64_t s_bytes = (uint64_t)vocab * (uint64_t)hidden / 16;
+    if (overlaps(out_bf16, out_bytes, ids, (uint64_t)num_ids * 8) ||
+        overlaps(out_bf16, out_bytes, weight, w_bytes) ||
+        overlaps(out_bf16, out_bytes, block_scale_e4m3, s_bytes) ||
+        overlaps(out_bf16, out_bytes, global_scale, 4) ||
+        (err_flag != nullptr &&
+         (overlaps(err_flag, 4, out_bf16, out_bytes) || overlaps(err_flag, 4, ids, num_ids * 8) ||
+          overlaps(err_flag, 4, weight, w_bytes) ||
+          overlaps(err_flag, 4, block_scale_e4m3, s_bytes) ||
+          overlaps(err_flag, 4, global_scale, 4))))
+        return FP4_ERR_ALIAS;
+    const void *ptrs[] = {ids, weight, block_scale_e4m3, global_scale, out_bf16, err_flag};
+    const fp4_status s = check_pointers(ptrs, 6);
+    if (s != FP4_OK) return s;
+    const cudaError_t err =
+        fp4mx::launch_nv_gather(ids, num_ids, weight, block_scale_e4m3, global_scale, vocab,
+                                hidden, out_bf16, err_flag, (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_nv_embedding_gather launch");
+}
+
+FP4_EXPORT const char *fp4_status_string(fp4_status status) {
+    switch (status) {
+    case FP4_OK: return "ok";
+    case FP4_ERR_NULL_PTR: return "a required pointer is NULL";
+    case FP4_ERR_SHAPE: return "invalid shape (negative size, k % 32 != 0, or size overflow)";
+    case FP4_ERR_GROUP: return "hidden size is not a multiple of group_size";
+    case FP4_ERR_UNSUPPORTED: return "unsupported group_size (NVFP4 uses 16)";
+    case FP4_ERR_INDEX: return "token id outside [0, vocab)";
+    case FP4_ERR_CUDA: return "CUDA runtime error";
+    case FP4_ERR_POINTER: return "pointer is not device-accessible CUDA memory";
+    case FP4_ERR_ALIAS: return "output overlaps an input";
+    }
+    return "unknown status";
+}
+
+FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
+
+FP4_EXPORT int fp4_abi_version(void) { return 100; }

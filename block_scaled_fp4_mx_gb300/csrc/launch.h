@@ -1,0 +1,26 @@
+// launch.h -- internal kernel launchers behind the C ABI (not exported).
+// Arguments reaching these have been validated by api.cu: sizes are positive,
+// pointers are device-accessible and outputs do not overlap inputs.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace fp4mx {
+
+// Decode n_elems (a positive multiple of 32) MXFP4 codes.
+cudaError_t launch_mx_unpack(const uint8_t *packed, const uint8_t *scales, uint16_t *out,
+                             int64_t n_elems, cudaStream_t stream);
+
+// Gather-dequant num_ids (> 0) rows of `hidden` (a positive multiple of 16) codes.
+cudaError_t launch_nv_gather(const int64_t *ids, int64_t num_ids, const uint8_t *weight,
+                             const uint8_t *scales, const float *global_scale, int64_t vocab,
+                             int64_t hidden, uint16_t *out, int32_t *err_flag,
+                             cudaStream_t stream);
+
+// Resident CTAs per SM x SM count for `kernel` at `threads` threads, cached per
+// device; a grid no larger than this runs in one wave.
+int max_resident_ctas(const void *kernel, int threads, int slot);
+
+}  // namespace fp4mx

@@ -124,13 +124,17 @@ def e8m0_choice(rng: np.random.Generator, n: int, values) -> np.ndarray:
 
 
 # Nibble draw for the stress stream: 200 equally likely outcomes, 30 -> code 0x0,
-# 30 -> code 0x8, and 10 for each of the 14 nonzero codes (1..7, 9..15).
+# 30 -> code 0x8, and 10 for each of the 14 nonzero codes (1..7, 9..15). A byte
+# is one uniform draw over 200 x 200 outcomes (low nibble = draw % 200, high
+# nibble = draw // 200), i.e. two independent nibble draws, looked up in a table.
 _NONZERO_CODES = np.array([1, 2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15], dtype=np.uint8)
-_STRESS_TABLE = np.concatenate([
+_STRESS_NIBBLE = np.concatenate([
     np.zeros(30, dtype=np.uint8),
     np.full(30, 8, dtype=np.uint8),
     np.tile(_NONZERO_CODES, 10),
 ])
+_STRESS_BYTE = (_STRESS_NIBBLE[np.arange(40000) % 200]
+                | (_STRESS_NIBBLE[np.arange(40000) // 200] << 4)).astype(np.uint8)
 
 
 def packed_with_zero_fraction(rng: np.random.Generator, n_bytes: int) -> np.ndarray:
@@ -139,9 +143,8 @@ def packed_with_zero_fraction(rng: np.random.Generator, n_bytes: int) -> np.ndar
     out = np.empty(n_bytes, dtype=np.uint8)
     for s in range(0, n_bytes, _CHUNK):
         e = min(n_bytes, s + _CHUNK)
-        draw = rng.integers(0, _STRESS_TABLE.size, size=2 * (e - s), dtype=np.uint8)
-        nib = _STRESS_TABLE[draw]
-        out[s:e] = nib[0::2] | (nib[1::2] << 4)
+        draw = rng.integers(0, _STRESS_BYTE.size, size=e - s, dtype=np.uint16)
+        out[s:e] = _STRESS_BYTE[draw]
     return out
 
 

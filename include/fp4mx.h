@@ -1,0 +1,135 @@
+/*
+ * fp4mx.h -- C ABI of a GB300 (sm_103a) library that decodes block-scaled FP4
+ * (E2M1) data into bf16.
+ *
+ * Two operations, each one CUDA kernel launch on the caller's stream:
+ *
+ *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
+ *                             a wrapping 16-bit integer add into the bf16 exponent
+ *                             field; both zero codes become +0.0.
+ *   fp4_nv_embedding_gather   NVFP4 embedding lookup: token ids pick rows of packed
+ *                             codes and of e4m3 scales (one per 16 codes); each
+ *                             value is multiplied by (block scale * global scale)
+ *                             in fp32 and rounded to bf16 (nearest, ties to even).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named "device" must be device-accessible CUDA allocations
+ *     (cudaMalloc / PyTorch CUDA tensors, or managed memory). Host pointers that
+ *     CUDA does not know return FP4_ERR_POINTER before anything is launched.
+ *   - bf16 values are passed as their 16-bit patterns (uint16_t).
+ *   - Element order inside a byte: the even element is the low nibble, the odd
+ *     element the high nibble.
+ *   - The caller owns every buffer. The library allocates, frees and
+ *     synchronises nothing; a call only enqueues work on `stream` (NULL = the
+ *     legacy default stream) and returns. Kernel faults surface at the caller's
+ *     next synchronisation, as with any CUDA launch.
+ *   - Arguments are checked on the host before any launch. On any error status
+ *     nothing is launched and the outputs are untouched. A call with zero
+ *     elements returns FP4_OK without launching.
+ *   - Outputs must not overlap inputs (FP4_ERR_ALIAS).
+ *   - Any alignment is accepted; 16-byte aligned outputs with 4-byte aligned
+ *     packed inputs take the vectorised kernels, others a scalar kernel with the
+ *     same results.
+ *   - Calls are thread-safe and may be captured into CUDA graphs (no host
+ *     synchronisation, no allocation, no host-to-device copy).
+ */
+#ifndef FP4MX_H
+#define FP4MX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *fp4_stream_t;
+
+typedef enum fp4_status {
+    FP4_OK = 0,
+    FP4_ERR_NULL_PTR = 1,    /* a required pointer is NULL                          */
+    FP4_ERR_SHAPE = 2,       /* negative size, k % 32 != 0, or size overflow        */
+    FP4_ERR_GROUP = 3,       /* hidden % group_size != 0                            */
+    FP4_ERR_UNSUPPORTED = 4, /* group_size other than 16                           */
+    FP4_ERR_INDEX = 5,       /* value written to err_flag when an id is out of range */
+    FP4_ERR_CUDA = 6,        /* the CUDA runtime reported an error (see fp4_last_error) */
+    FP4_ERR_POINTER = 7,     /* a pointer is not device-accessible memory           */
+    FP4_ERR_ALIAS = 8        /* an output range overlaps an input range             */
+} fp4_status;
+
+/*
+ * fp4_mx_unpack -- MXFP4 (E2M1 codes, E8M0 per-32 scale) to bf16.
+ *
+ * Defined by "vllm-project/vllm pull 51583" (prhub digest), sections
+ * "Motivation" and "Implementation breakdown": the E8M0 block scale is applied
+ * as an integer add into the bf16 exponent field, and the two zero codes (+0.0,
+ * -0.0) are forced to +0.0 lane by lane. With E the scale byte of element j's
+ * block (j / 32) and L the bf16 pattern of the code's E2M1 value:
+ *     out[j] = (L & 0x7FFF) != 0 ? (L + ((E - 127) << 7)) mod 2^16 : 0x0000
+ * The add wraps: every E in 0..255 is a plain exponent (255 is not NaN), and
+ * exponents that leave the bf16 range give the wrapped bit pattern.
+ *
+ *   packed       device, uint8[rows * k / 2], row-major [rows, k/2]
+ *   scales_e8m0  device, uint8[rows * k / 32], row-major [rows, k/32]
+ *   out_bf16     device, uint16[rows * k], row-major [rows, k]
+ *   rows, k      rows >= 0, k >= 0, k % 32 == 0 (else FP4_ERR_SHAPE)
+ *   stream       CUDA stream the kernel is enqueued on
+ *
+ * Rows are contiguous, so the data is one stream of rows * k codes; element j
+ * reads byte j / 2 and scale byte j / 32.
+ */
+fp4_status fp4_mx_unpack(const uint8_t *packed, const uint8_t *scales_e8m0, uint16_t *out_bf16,
+                         int64_t rows, int64_t k, fp4_stream_t stream);
+
+/*
+ * fp4_nv_embedding_gather -- NVFP4 token-embedding lookup, dequantised while
+ * gathering.
+ *
+ * Defined by "sgl-project/sglang pull 34222" (prhub digest), sections
+ * "Implementation breakdown" (items 1-2) and "Key source snippets"
+ * (ModelOptNvFp4EmbeddingMethod.embedding, create_weights, reference_dequant):
+ * for token t with id = ids[t] and column c,
+ *     code = nibble c of weight[id]           (even c: low nibble, odd c: high)
+ *     v    = (code & 8 ? -1 : +1) * {0, 0.5, 1, 1.5, 2, 3, 4, 6}[code & 7]
+ *     eff  = fp32(e4m3 block_scale[id][c / 16]) * global_scale      (fp32, RNE)
+ *     out[t][c] = bf16_rne(v * eff)                                  (fp32, RNE)
+ * No fused multiply-add; code 8 gives -0.0 * eff (a signed zero is kept).
+ *
+ *   ids              device, int64[num_ids] (any logical shape, flattened)
+ *   num_ids          >= 0
+ *   weight           device, uint8[vocab * hidden / 2], row-major [vocab, hidden/2]
+ *   block_scale_e4m3 device, uint8[vocab * hidden / 16] float8 e4m3fn bit patterns,
+ *                    row-major [vocab, hidden/16]
+ *   global_scale     device, one fp32 (a device pointer so that no host read or
+ *                    synchronisation is needed and the call can be graph-captured)
+ *   vocab            >= 1 when num_ids > 0
+ *   hidden           > 0, hidden % group_size == 0 (else FP4_ERR_GROUP, the check
+ *                    the pages' create_weights performs)
+ *   group_size       must be 16 (NVFP4); other positive values: FP4_ERR_UNSUPPORTED
+ *   out_bf16         device, uint16[num_ids * hidden], row-major [num_ids, hidden]
+ *   err_flag         device int32 or NULL. An id outside [0, vocab) never faults:
+ *                    its output row is written as +0.0 and, when err_flag is not
+ *                    NULL, *err_flag is set to FP4_ERR_INDEX (never cleared by the
+ *                    library; the caller zeroes it and reads it when it syncs).
+ *   stream           CUDA stream the kernel is enqueued on
+ */
+fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_ids, const uint8_t *weight,
+                                   const uint8_t *block_scale_e4m3, const float *global_scale,
+                                   int64_t vocab, int64_t hidden, int64_t group_size,
+                                   uint16_t *out_bf16, int32_t *err_flag, fp4_stream_t stream);
+
+/* Static English text for a status code ("unknown status" for other values). */
+const char *fp4_status_string(fp4_status status);
+
+/* Text of the last CUDA error this thread's calls met ("" if none). Valid
+ * until this thread's next call into the library. */
+const char *fp4_last_error(void);
+
+/* Version of this ABI (major * 100 + minor). */
+int fp4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4MX_H */

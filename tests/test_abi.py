@@ -1,0 +1,97 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and
+rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_fp4_mx_gb300 as fp4
+from block_scaled_fp4_mx_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(fp4_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return fp4.load()
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("fp4_mx_unpack", "fp4_nv_embedding_gather", "fp4_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_only_api_symbols_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", fp4.library_path()],
+                         capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm unavailable")
+    syms = [l.split()[-1] for l in out.stdout.splitlines() if l.strip()]
+    public = [s for s in syms if not s.startswith("_")]
+    assert sorted(p for p in public if p.startswith("fp4_")) == declared_functions()
+
+
+def test_status_strings(lib):
+    assert fp4.fp4_status_string(0) == "ok"
+    for code in range(1, 9):
+        assert fp4.fp4_status_string(code) not in ("", "unknown status")
+    assert fp4.fp4_status_string(99) == "unknown status"
+    assert lib.fp4_abi_version() == 100
+
+
+def test_mx_host_validation(lib):
+    f = lib.fp4_mx_unpack
+    assert f(None, None, None, 1, 33, None) == fp4.Status.ERR_SHAPE      # k % 32
+    assert f(None, None, None, -1, 32, None) == fp4.Status.ERR_SHAPE
+    assert f(None, None, None, 1, -32, None) == fp4.Status.ERR_SHAPE
+    assert f(None, None, None, 0, 64, None) == fp4.Status.OK             # empty: no launch
+    assert f(None, None, None, 5, 0, None) == fp4.Status.OK
+    assert f(None, None, None, 2, 64, None) == fp4.Status.ERR_NULL_PTR
+    assert f(None, None, None, 2 ** 62, 2 ** 10, None) == fp4.Status.ERR_SHAPE  # overflow
+    # output overlapping the input is refused before any CUDA call
+    buf = ctypes.create_string_buffer(4096)
+    base = ctypes.addressof(buf)
+    assert f(base, base + 2048, base + 16, 1, 64, None) == fp4.Status.ERR_ALIAS
+
+
+def test_nv_host_validation(lib):
+    f = lib.fp4_nv_embedding_gather
+    args = lambda n, v, h, g: (None, n, None, None, None, v, h, g, None, None, None)
+    assert f(*args(4, 10, 100, 16)) == fp4.Status.ERR_GROUP       # hidden % group_size
+    assert f(*args(4, 10, 96, 32)) == fp4.Status.ERR_UNSUPPORTED  # NVFP4 groups are 16
+    assert f(*args(4, 10, 0, 16)) == fp4.Status.ERR_SHAPE
+    assert f(*args(-1, 10, 64, 16)) == fp4.Status.ERR_SHAPE
+    assert f(*args(4, 10, 64, 0)) == fp4.Status.ERR_SHAPE
+    assert f(*args(0, 10, 64, 16)) == fp4.Status.OK               # no ids: no launch
+    assert f(*args(4, 0, 64, 16)) == fp4.Status.ERR_SHAPE         # ids but empty table
+    assert f(*args(4, 10, 64, 16)) == fp4.Status.ERR_NULL_PTR
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError, match="CUDA"):
+        fp4.fp4_mx_unpack(torch.zeros(2, 16, dtype=torch.uint8), torch.zeros(2, 1, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="CUDA"):
+        fp4.fp4_nv_embedding_gather(torch.zeros(3, dtype=torch.int64),
+                                    torch.zeros(4, 8, dtype=torch.uint8),
+                                    torch.zeros(4, 1, dtype=torch.uint8),
+                                    torch.ones(1, dtype=torch.float32))

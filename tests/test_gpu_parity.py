@@ -1,0 +1,328 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit for bit.
+
+Tolerance is zero for both entry points (bf16 bit patterns compared as uint16):
+MXFP4 is integer work, and NVFP4 fixes its fp32 op order and rounding, so both
+sides take every rounding decision in the same precision. NaN (only from the e4m3
+NaN scale byte, outside the workloads) is compared as "both NaN".
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import block_scaled_fp4_mx_gb300 as fp4
+from block_scaled_fp4_mx_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+THREADS = 0  # oracle threads: 0 -> all host cores
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.fixture(scope="module")
+def ref(oracle_impl):
+    global THREADS
+    THREADS = oracle_impl.max_threads()
+    return oracle_impl
+
+
+def bits(t) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def assert_same(got: np.ndarray, want: np.ndarray, what: str):
+    got, want = got.reshape(-1), want.reshape(-1)
+    assert got.shape == want.shape, what
+    if not np.array_equal(got, want):
+        diff = np.nonzero(got != want)[0]
+        i = int(diff[0])
+        raise AssertionError(f"{what}: {diff.size} mismatches, first at {i}: "
+                             f"gpu {got[i]:#06x} oracle {want[i]:#06x}")
+
+
+def gpu_mx(x, out=None):
+    p = torch.from_numpy(x.packed).to(DEV)
+    s = torch.from_numpy(x.scales).to(DEV)
+    return fp4.fp4_mx_unpack(p, s, out=out)
+
+
+def gpu_nv(x, err=None, ids=None):
+    ids = x.ids if ids is None else ids
+    return fp4.fp4_nv_embedding_gather(
+        torch.from_numpy(np.ascontiguousarray(ids)).to(DEV), torch.from_numpy(x.weight).to(DEV),
+        torch.from_numpy(x.scales).to(DEV),
+        torch.tensor([x.global_scale], dtype=torch.float32, device=DEV), err_flag=err)
+
+
+# ---------------------------------------------------------------------------
+# MXFP4
+# ---------------------------------------------------------------------------
+
+def test_mx_exhaustive(ref):
+    """Every packed byte x every E8M0 exponent, once each."""
+    x = inputs.mx_exhaustive()
+    assert_same(bits(gpu_mx(x)), ref.mx_unpack(x.packed, x.scales), "mx exhaustive")
+
+
+def test_mx_pages_zero_codes(ref):
+    """The pages' zero bytes x exponents, as whole blocks: exactly +0.0."""
+    for zb in (0x00, 0x88, 0x08, 0x80):
+        for e in (0, 1, 127, 200, 254, 255):
+            x = inputs.MxInput(np.full((4, 64), zb, np.uint8), np.full((4, 4), e, np.uint8))
+            assert np.all(bits(gpu_mx(x)) == 0)
+
+
+@pytest.mark.parametrize("rows,k,seed", [(1, 32, 1), (3, 64, 2), (7, 2880, 3), (33, 4096, 4),
+                                         (1, 1024 * 32 + 32, 5), (129, 96, 6), (2048, 2880, 7)])
+def test_mx_random_shapes(ref, rows, k, seed):
+    """Several tiles, a ragged tail (word count not a multiple of the CTA chunk),
+    random exponents over 0..255 and a 30% share of zero codes."""
+    x = inputs.mx_random(rows, k, seed, zero_fraction=(seed % 2 == 0))
+    assert_same(bits(gpu_mx(x)), ref.mx_unpack(x.packed, x.scales, THREADS), f"mx {rows}x{k}")
+
+
+def test_mx_leading_dims_and_empty(ref):
+    x = inputs.mx_random(6, 64, seed=9)
+    p = torch.from_numpy(x.packed.reshape(2, 3, 32)).to(DEV)
+    s = torch.from_numpy(x.scales.reshape(2, 3, 2)).to(DEV)
+    out = fp4.fp4_mx_unpack(p, s)
+    assert out.shape == (2, 3, 64)
+    assert_same(bits(out), ref.mx_unpack(x.packed, x.scales), "mx 3-d")
+    empty = fp4.fp4_mx_unpack(torch.empty(0, 16, dtype=torch.uint8, device=DEV),
+                              torch.empty(0, 1, dtype=torch.uint8, device=DEV))
+    assert empty.shape == (0, 32)
+
+
+@pytest.mark.parametrize("p_off,o_off", [(1, 0), (0, 2), (3, 6), (2, 8)])
+def test_mx_unaligned_buffers(ref, p_off, o_off):
+    """Buffers that are not 4 / 16-byte aligned take the byte kernel: same bits."""
+    x = inputs.mx_random(5, 352, seed=10 + p_off, zero_fraction=True)
+    n = x.n_elems
+    pbuf = torch.zeros(x.packed.size + 16, dtype=torch.uint8, device=DEV)
+    pbuf[p_off:p_off + x.packed.size] = torch.from_numpy(x.packed.reshape(-1)).to(DEV)
+    obuf = torch.zeros(2 * n + 32, dtype=torch.uint8, device=DEV)
+    out = obuf[o_off:o_off + 2 * n].view(torch.uint8)
+    lib = fp4.load()
+    s = torch.from_numpy(x.scales).to(DEV)
+    code = lib.fp4_mx_unpack(ctypes.c_void_p(pbuf.data_ptr() + p_off), ctypes.c_void_p(s.data_ptr()),
+                             ctypes.c_void_p(obuf.data_ptr() + o_off), x.rows, x.k,
+                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    got = out.cpu().numpy().view(np.uint16)
+    assert_same(got, ref.mx_unpack(x.packed, x.scales), "mx unaligned")
+
+
+def test_mx_output_canaries(ref):
+    """Nothing is written outside the output range."""
+    x = inputs.mx_random(17, 320, seed=12)
+    n = x.n_elems
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 0x5A5A, dtype=torch.int16, device=DEV)
+    out = buf[guard:guard + n].view(torch.bfloat16).view(17, 320)
+    gpu_mx(x, out=out)
+    host = buf.cpu().numpy().view(np.uint16)
+    assert np.all(host[:guard] == 0x5A5A) and np.all(host[guard + n:] == 0x5A5A)
+    assert_same(host[guard:guard + n], ref.mx_unpack(x.packed, x.scales), "mx canary")
+
+
+def test_mx_errors_through_binding():
+    p = torch.zeros(4, 16, dtype=torch.uint8, device=DEV)
+    s = torch.zeros(4, 1, dtype=torch.uint8, device=DEV)
+    lib = fp4.load()
+    host = (ctypes.c_uint8 * 64)()
+    # a plain host pointer is refused before any launch
+    code = lib.fp4_mx_unpack(ctypes.addressof(host), s.data_ptr(),
+                             torch.empty(4, 32, dtype=torch.bfloat16, device=DEV).data_ptr(),
+                             4, 32, None)
+    assert code == fp4.Status.ERR_POINTER
+    out = torch.empty(4, 32, dtype=torch.bfloat16, device=DEV)
+    alias = lib.fp4_mx_unpack(out.data_ptr(), s.data_ptr(), out.data_ptr(), 4, 32, None)
+    assert alias == fp4.Status.ERR_ALIAS
+    with pytest.raises(ValueError):
+        fp4.fp4_mx_unpack(p, torch.zeros(4, 2, dtype=torch.uint8, device=DEV))
+
+
+# full-size workloads, compared in full (the oracle runs on all host cores)
+
+def test_mx_moe_full(ref):
+    for x in inputs.mx_moe():
+        out = gpu_mx(x)
+        assert_same(bits(out), ref.mx_unpack(x.packed, x.scales, THREADS), x.name)
+        del out
+
+
+def test_mx_stress_full(ref):
+    x = inputs.mx_stress()
+    out = gpu_mx(x)
+    got = bits(out)
+    del out
+    torch.cuda.empty_cache()
+    assert_same(got, ref.mx_unpack(x.packed, x.scales, THREADS), x.name)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4
+# ---------------------------------------------------------------------------
+
+def nv_check(ref, x, what, ids=None):
+    ids = x.ids if ids is None else ids
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = gpu_nv(x, err, ids)
+    want, bad = ref.nv_embedding_gather(ids, x.weight, x.scales, x.global_scale, threads=THREADS)
+    assert tuple(out.shape) == want.shape
+    assert_same(bits(out), want, what)
+    assert int(err.item()) == (fp4.Status.ERR_INDEX if bad else 0)
+    return bad
+
+
+def test_nv_embedding_32k(ref):
+    x = inputs.nv_embedding_32k()
+    assert nv_check(ref, x, x.name) == 0
+
+
+def test_nv_embedding_200k_full(ref):
+    x = inputs.nv_embedding_200k()
+    assert nv_check(ref, x, x.name) == 0
+
+
+@pytest.mark.parametrize("vocab,hidden,shape,seed", [
+    (1, 16, (1,), 1), (5, 32, (9,), 2), (64, 2880, (3, 5), 3), (100, 4096 + 16, (17,), 4),
+    (300, 8192, (2, 2, 3), 5), (7, 48, (0,), 6)])
+def test_nv_shapes(ref, vocab, hidden, shape, seed):
+    """One-group rows, ragged segments (hidden 2880 -> 360 words), id shapes of
+    several ranks, and no ids at all."""
+    x = inputs.nv_random(vocab, hidden, shape, seed)
+    nv_check(ref, x, f"nv {vocab}x{hidden}")
+
+
+@pytest.mark.parametrize("gs", [1.0, 0.37, 1e-36, 3.0e4, -0.5])
+def test_nv_global_scales(ref, gs):
+    """Global scales other than 1/448, including a negative one (signs of zeros
+    flip) and ones that take products to bf16 subnormals / large values."""
+    x = inputs.nv_random(50, 256, (40,), seed=7, global_scale=np.float32(gs))
+    nv_check(ref, x, f"nv gs={gs}")
+
+
+def test_nv_every_scale_byte(ref):
+    """Every e4m3 byte as a block scale (NaN bytes compared as NaN)."""
+    codes = np.arange(16, dtype=np.uint8)
+    w_row = np.tile(codes[0::2] | (codes[1::2] << 4), 2)  # hidden 32
+    weight = np.tile(w_row[None, :], (256, 1))
+    scales = np.stack([np.arange(256), np.arange(256)], axis=1).astype(np.uint8)
+    x = inputs.NvInput(np.arange(256, dtype=np.int64), weight, scales, np.float32(1.0 / 3))
+    out = bits(gpu_nv(x))
+    want, _ = ref.nv_embedding_gather(x.ids, weight, scales, x.global_scale)
+    nan_rows = np.array([b for b in range(256) if (b & 0x7F) == 0x7F])
+    finite = np.setdiff1d(np.arange(256), nan_rows)
+    assert_same(out[finite], want[finite], "nv all scale bytes")
+    is_nan = lambda b: ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+    assert np.all(is_nan(out[nan_rows][:, [1, 2, 3, 9]]) == is_nan(want[nan_rows][:, [1, 2, 3, 9]]))
+
+
+def test_nv_out_of_range_ids(ref):
+    """Bad ids give +0.0 rows and set the error flag; good rows are untouched."""
+    x = inputs.nv_random(20, 2880, (6,), seed=8)
+    ids = np.array([3, -1, 20, 19, -(2 ** 40), 0], dtype=np.int64)
+    assert nv_check(ref, x, "nv bad ids", ids=ids) == 3
+
+
+def test_nv_repeated_ids_and_dense(ref):
+    x = inputs.nv_random(12, 64, (1,), seed=9)
+    dense = bits(gpu_nv(x, ids=np.arange(12)))
+    rep = bits(gpu_nv(x, ids=np.array([[5, 5], [11, 5]])))
+    assert rep.shape == (2, 2, 64)
+    assert np.array_equal(rep[0, 0], dense[5]) and np.array_equal(rep[1, 0], dense[11])
+    assert np.array_equal(rep[0, 1], rep[1, 1])
+
+
+@pytest.mark.parametrize("w_off,o_off", [(1, 0), (0, 2), (2, 6)])
+def test_nv_unaligned_buffers(ref, w_off, o_off):
+    x = inputs.nv_random(30, 160, (11,), seed=20 + w_off)
+    lib = fp4.load()
+    wbuf = torch.zeros(x.weight.size + 16, dtype=torch.uint8, device=DEV)
+    wbuf[w_off:w_off + x.weight.size] = torch.from_numpy(x.weight.reshape(-1)).to(DEV)
+    obuf = torch.zeros(x.ids.size * x.hidden * 2 + 32, dtype=torch.uint8, device=DEV)
+    ids = torch.from_numpy(x.ids).to(DEV)
+    s = torch.from_numpy(x.scales).to(DEV)
+    gs = torch.tensor([x.global_scale], dtype=torch.float32, device=DEV)
+    code = lib.fp4_nv_embedding_gather(ids.data_ptr(), x.ids.size, wbuf.data_ptr() + w_off,
+                                       s.data_ptr(), gs.data_ptr(), x.vocab, x.hidden, 16,
+                                       obuf.data_ptr() + o_off, None,
+                                       torch.cuda.current_stream().cuda_stream)
+    assert code == 0
+    got = obuf[o_off:o_off + x.ids.size * x.hidden * 2].cpu().numpy().view(np.uint16)
+    want, _ = ref.nv_embedding_gather(x.ids, x.weight, x.scales, x.global_scale)
+    assert_same(got, want, "nv unaligned")
+
+
+def test_nv_output_canaries(ref):
+    x = inputs.nv_random(40, 2880, (13,), seed=21)
+    n = x.n_elems
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 0x5A5A, dtype=torch.int16, device=DEV)
+    out = buf[guard:guard + n].view(torch.bfloat16).view(13, 2880)
+    fp4.fp4_nv_embedding_gather(torch.from_numpy(x.ids).to(DEV), torch.from_numpy(x.weight).to(DEV),
+                                torch.from_numpy(x.scales).to(DEV),
+                                torch.tensor([x.global_scale], device=DEV), out=out)
+    host = buf.cpu().numpy().view(np.uint16)
+    assert np.all(host[:guard] == 0x5A5A) and np.all(host[guard + n:] == 0x5A5A)
+    want, _ = ref.nv_embedding_gather(x.ids, x.weight, x.scales, x.global_scale)
+    assert_same(host[guard:guard + n], want, "nv canary")
+
+
+def test_nv_guards_through_binding():
+    w = torch.zeros(4, 50, dtype=torch.uint8, device=DEV)  # hidden 100
+    s = torch.zeros(4, 6, dtype=torch.uint8, device=DEV)
+    ids = torch.zeros(2, dtype=torch.int64, device=DEV)
+    gs = torch.ones(1, device=DEV)
+    with pytest.raises(fp4.Fp4Error) as e:
+        fp4.fp4_nv_embedding_gather(ids, w, s, gs)
+    assert e.value.code == fp4.Status.ERR_GROUP
+    w = torch.zeros(4, 48, dtype=torch.uint8, device=DEV)  # hidden 96
+    with pytest.raises(fp4.Fp4Error) as e:
+        fp4.fp4_nv_embedding_gather(ids, w, torch.zeros(4, 3, dtype=torch.uint8, device=DEV), gs,
+                                    group_size=32)
+    assert e.value.code == fp4.Status.ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# streams and graphs
+# ---------------------------------------------------------------------------
+
+def test_side_stream_and_graph_capture(ref):
+    """Both calls enqueue on the given stream and can be captured in a CUDA graph."""
+    xm = inputs.mx_random(64, 2880, seed=30)
+    xn = inputs.nv_random(500, 4096, (64,), seed=31)
+    p, s = torch.from_numpy(xm.packed).to(DEV), torch.from_numpy(xm.scales).to(DEV)
+    ids, w = torch.from_numpy(xn.ids).to(DEV), torch.from_numpy(xn.weight).to(DEV)
+    sc = torch.from_numpy(xn.scales).to(DEV)
+    gs = torch.tensor([xn.global_scale], device=DEV)
+    out_m = torch.empty(64, 2880, dtype=torch.bfloat16, device=DEV)
+    out_n = torch.empty(64, 4096, dtype=torch.bfloat16, device=DEV)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        fp4.fp4_mx_unpack(p, s, out=out_m)
+        fp4.fp4_nv_embedding_gather(ids, w, sc, gs, out=out_n)
+    side.synchronize()
+    want_m = ref.mx_unpack(xm.packed, xm.scales)
+    want_n, _ = ref.nv_embedding_gather(xn.ids, xn.weight, xn.scales, xn.global_scale)
+    assert_same(bits(out_m), want_m, "side stream mx")
+    assert_same(bits(out_n), want_n, "side stream nv")
+    out_m.zero_()
+    out_n.zero_()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fp4.fp4_mx_unpack(p, s, out=out_m)
+        fp4.fp4_nv_embedding_gather(ids, w, sc, gs, out=out_n)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same(bits(out_m), want_m, "graph mx")
+    assert_same(bits(out_n), want_n, "graph nv")
