@@ -7,8 +7,12 @@
 //
 // A warp owns one segment of one output row (up to 32 * kUnroll words = 256 *
 // kUnroll codes), so each row is read with coalesced 128-byte warp loads and
-// written with 512-byte warp stores; rows are cut into segments so that a
-// persistent grid of warps balances even when there are fewer rows than warps.
+// written with 512-byte warp stores, with kUnroll loads in flight per lane.
+// The grid is one-shot (one warp per segment): the block scheduler keeps the
+// CTAs in flight on a compact, advancing window of the output, which measured
+// faster on GB300 than a persistent grid-stride loop. Rows narrower than 32
+// words take a flat kernel (one thread per word of the [num_ids, hidden]
+// output) so that lanes are not left idle.
 // An id outside [0, vocab) never faults: its row is written as +0.0 and the
 // caller's error flag is set.
 #include "fp4_decode.cuh"
@@ -21,53 +25,77 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;
-constexpr int64_t kSegWords = 32 * kUnroll;
+constexpr uint32_t kSegWords = 32 * kUnroll;
 
+// Warp per (row, segment). Rows are [0, num_rows) of this launch; unit = row *
+// segs_per_row + segment fits in 32 bits (the launcher splits larger calls).
 __global__ void __launch_bounds__(kThreads)
-nv_gather_words_kernel(const int64_t *__restrict__ ids, int64_t num_ids,
-                       const uint32_t *__restrict__ weight, const uint8_t *__restrict__ scales,
-                       const float *__restrict__ global_scale, int64_t vocab,
-                       int64_t words_per_row, int64_t segs_per_row, uint4 *__restrict__ out,
-                       int32_t *__restrict__ err_flag) {
+nv_gather_rows_kernel(const int64_t *__restrict__ ids, uint32_t n_units,
+                      const uint32_t *__restrict__ weight, const uint8_t *__restrict__ scales,
+                      const float *__restrict__ global_scale, int64_t vocab,
+                      uint32_t words_per_row, uint32_t segs_per_row, uint4 *__restrict__ out,
+                      int32_t *__restrict__ err_flag) {
+    const uint32_t unit = blockIdx.x * (uint32_t)kWarps + (threadIdx.x >> 5);
+    if (unit >= n_units) return;
     const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t n_warps = ((int64_t)gridDim.x * kThreads) >> 5;
-    const int64_t n_units = num_ids * segs_per_row;
-    const int64_t groups_per_row = words_per_row / 2;  // 2 words per 16-code group
-    const float gs = __ldg(global_scale);
-    for (int64_t unit = warp; unit < n_units; unit += n_warps) {
-        const int64_t t = unit / segs_per_row;
-        const int64_t w0 = (unit - t * segs_per_row) * kSegWords;
-        const int64_t id = __ldg(ids + t);
-        uint4 *out_row = out + t * words_per_row;
-        if (id < 0 || id >= vocab) {
+    const uint32_t t = unit / segs_per_row;
+    const uint32_t w0 = (unit - t * segs_per_row) * kSegWords;
+    const int64_t id = __ldg(ids + t);
+    uint4 *out_row = out + (int64_t)t * words_per_row;
+    if (id < 0 || id >= vocab) {
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t i = w0 + u * 32 + lane;
-                if (i < words_per_row) st_stream(out_row + i, make_uint4(0, 0, 0, 0));
-            }
-            if (w0 == 0 && lane == 0 && err_flag != nullptr) atomicExch(err_flag, FP4_ERR_INDEX);
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t i = w0 + u * 32 + lane;
+            if (i < words_per_row) st_stream(out_row + i, make_uint4(0, 0, 0, 0));
+        }
+        if (w0 == 0 && lane == 0 && err_flag != nullptr) atomicExch(err_flag, FP4_ERR_INDEX);
+        return;
+    }
+    const float gs = __ldg(global_scale);
+    const uint32_t *w_row = weight + id * words_per_row;
+    const uint8_t *s_row = scales + id * (words_per_row / 2);  // 2 words per 16-code group
+    uint32_t w[kUnroll], s[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t i = w0 + u * 32 + lane;
+        if (i < words_per_row) {
+            w[u] = __ldg(w_row + i);
+            s[u] = __ldg(s_row + (i >> 1));
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t i = w0 + u * 32 + lane;
+        if (i < words_per_row)
+            st_stream(out_row + i, nv_decode_word(w[u], __fmul_rn(e4m3_to_f32(s[u]), gs)));
+    }
+}
+
+// Thread per word of the flattened [num_rows, words_per_row] output, kUnroll
+// words per thread strided by kThreads (for rows narrower than a warp's loads).
+__global__ void __launch_bounds__(kThreads)
+nv_gather_flat_kernel(const int64_t *__restrict__ ids, int64_t n_words,
+                      const uint32_t *__restrict__ weight, const uint8_t *__restrict__ scales,
+                      const float *__restrict__ global_scale, int64_t vocab,
+                      uint32_t words_per_row, uint4 *__restrict__ out,
+                      int32_t *__restrict__ err_flag) {
+    const int64_t base = (int64_t)blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
+    const float gs = __ldg(global_scale);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int64_t f = base + u * kThreads;
+        if (f >= n_words) continue;
+        const int64_t t = f / words_per_row;
+        const uint32_t i = (uint32_t)(f - t * words_per_row);
+        const int64_t id = __ldg(ids + t);
+        if (id < 0 || id >= vocab) {
+            st_stream(out + f, make_uint4(0, 0, 0, 0));
+            if (i == 0 && err_flag != nullptr) atomicExch(err_flag, FP4_ERR_INDEX);
             continue;
         }
-        const uint32_t *w_row = weight + id * words_per_row;
-        const uint8_t *s_row = scales + id * groups_per_row;
-        uint32_t w[kUnroll], s[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t i = w0 + u * 32 + lane;
-            if (i < words_per_row) {
-                w[u] = __ldg(w_row + i);
-                s[u] = __ldg(s_row + (i >> 1));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t i = w0 + u * 32 + lane;
-            if (i < words_per_row) {
-                const float eff = __fmul_rn(e4m3_to_f32(s[u]), gs);
-                st_stream(out_row + i, nv_decode_word(w[u], eff));
-            }
-        }
+        const uint32_t w = __ldg(weight + id * words_per_row + i);
+        const uint32_t sc = __ldg(scales + id * (words_per_row / 2) + (i >> 1));
+        st_stream(out + f, nv_decode_word(w, __fmul_rn(e4m3_to_f32(sc), gs)));
     }
 }
 
@@ -110,14 +138,32 @@ cudaError_t launch_nv_gather(const int64_t *ids, int64_t num_ids, const uint8_t 
                            (reinterpret_cast<uintptr_t>(out) % 16 == 0);
     if (vector_ok) {
         const int64_t words_per_row = hidden / 8;
-        const int64_t segs = (words_per_row + kSegWords - 1) / kSegWords;
-        const int64_t units = num_ids * segs;
-        const int64_t blocks = (units + kWarps - 1) / kWarps;
-        const int cap = max_resident_ctas((const void *)nv_gather_words_kernel, kThreads, 2);
-        const int grid = (int)(blocks < cap ? blocks : cap);
-        nv_gather_words_kernel<<<grid, kThreads, 0, stream>>>(
-            ids, num_ids, reinterpret_cast<const uint32_t *>(weight), scales, global_scale, vocab,
-            words_per_row, segs, reinterpret_cast<uint4 *>(out), err_flag);
+        if (words_per_row >= 32) {
+            // rows in pieces so that row * segments stays below 2^31
+            const int64_t segs = (words_per_row + kSegWords - 1) / kSegWords;
+            const int64_t rows_per_launch = ((int64_t)1 << 31) / segs;
+            for (int64_t r0 = 0; r0 < num_ids; r0 += rows_per_launch) {
+                const int64_t rows = num_ids - r0 < rows_per_launch ? num_ids - r0 : rows_per_launch;
+                const int64_t units = rows * segs;
+                const int grid = (int)((units + kWarps - 1) / kWarps);
+                nv_gather_rows_kernel<<<grid, kThreads, 0, stream>>>(
+                    ids + r0, (uint32_t)units, reinterpret_cast<const uint32_t *>(weight), scales,
+                    global_scale, vocab, (uint32_t)words_per_row, (uint32_t)segs,
+                    reinterpret_cast<uint4 *>(out) + r0 * words_per_row, err_flag);
+            }
+        } else {
+            constexpr int64_t kChunk = (int64_t)kThreads * kUnroll;
+            const int64_t rows_per_launch = ((int64_t)1 << 40) / words_per_row;
+            for (int64_t r0 = 0; r0 < num_ids; r0 += rows_per_launch) {
+                const int64_t rows = num_ids - r0 < rows_per_launch ? num_ids - r0 : rows_per_launch;
+                const int64_t n_words = rows * words_per_row;
+                const int grid = (int)((n_words + kChunk - 1) / kChunk);
+                nv_gather_flat_kernel<<<grid, kThreads, 0, stream>>>(
+                    ids + r0, n_words, reinterpret_cast<const uint32_t *>(weight), scales,
+                    global_scale, vocab, (uint32_t)words_per_row,
+                    reinterpret_cast<uint4 *>(out) + r0 * words_per_row, err_flag);
+            }
+        }
     } else {
         const int64_t n = num_ids * (hidden / 2);
         const int64_t blocks = (n + kThreads - 1) / kThreads;

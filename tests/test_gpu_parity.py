@@ -226,9 +226,11 @@ def test_nv_every_scale_byte(ref):
     assert np.all(is_nan(out[nan_rows][:, [1, 2, 3, 9]]) == is_nan(want[nan_rows][:, [1, 2, 3, 9]]))
 
 
-def test_nv_out_of_range_ids(ref):
-    """Bad ids give +0.0 rows and set the error flag; good rows are untouched."""
-    x = inputs.nv_random(20, 2880, (6,), seed=8)
+@pytest.mark.parametrize("hidden", [2880, 64])
+def test_nv_out_of_range_ids(ref, hidden):
+    """Bad ids give +0.0 rows and set the error flag; good rows are untouched
+    (row-segment kernel at hidden 2880, flat kernel at hidden 64)."""
+    x = inputs.nv_random(20, hidden, (6,), seed=8)
     ids = np.array([3, -1, 20, 19, -(2 ** 40), 0], dtype=np.int64)
     assert nv_check(ref, x, "nv bad ids", ids=ids) == 3
 
