@@ -6,7 +6,8 @@ MXFP4 unpack of an MoE expert stack (gate+up [32, 5760, 2880] and down
 [32, 2880, 2880] codes; two fp4_mx_unpack launches) plus an NVFP4 embedding
 gather-dequant (vocab 200,000 x hidden 8,192, 16,384 Zipf(1.1) ids as [64, 256];
 one fp4_nv_embedding_gather launch). ``--workload`` picks one of the other named
-workloads instead (one entry point per step).
+workloads instead (one entry point per step, e.g. ``nv_dequant_200k``: fp4_nv_dequant
+of the whole 200k x 8,192 table).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -14,7 +15,8 @@ Prints one JSON line (rank 0). ``value`` is decoded elements per second over all
 ranks with inputs resident in HBM; ``e2e`` is the same metric through the public
 API with pinned host buffers, the host->device copies of each step's inputs and
 the device->host copies of its outputs inside the timed region; ``roofline`` is
-the dominant kernel (the MXFP4 unpack) against the measured HBM copy bandwidth;
+the dominant kernel (most device time per step; the MXFP4 unpack by default)
+against the measured HBM copy bandwidth;
 ``cpu_baseline`` is the CPU oracle on a bounded sample of the same workload.
 With ``--impl reference`` the CPU oracle itself is timed on the same workload
 (a bounded sample per step) and reported as the reference arm.
@@ -44,8 +46,7 @@ METRIC = "decoded FP4 elements/sec and achieved HBM GB/s (% of GB300 peak), 1 GP
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("step", "mx_moe", "mx_stress", "mx_exhaustive", "nv_embedding_200k",
-             "nv_embedding_32k")
-DOMINANT = "mx_unpack"  # kernel the roofline object describes
+             "nv_embedding_32k", "nv_dequant_200k", "nv_dequant_32k")
 
 
 # ---------------------------------------------------------------------------
@@ -189,26 +190,157 @@ def _which(name):
 
 
 # ---------------------------------------------------------------------------
-# workloads
+# workloads: each op kind knows its launch, its bytes, its e2e chunks and its
+# oracle sample
 # ---------------------------------------------------------------------------
 
+class MxOp:
+    """fp4_mx_unpack of one [rows, k] tensor."""
+    kind, kernel = "mx_unpack", "mx_unpack_words_kernel"
+
+    def __init__(self, x):
+        self.x = x
+        self.elems = x.n_elems
+        self.bytes = x.algorithmic_bytes()
+        self.min_bytes = self.bytes
+        self.units, self.elems_per_unit = x.rows, x.k
+
+    def to_device(self, torch, dev):
+        x = self.x
+        self.p = torch.from_numpy(x.packed).to(dev)
+        self.s = torch.from_numpy(x.scales).to(dev)
+        self.o = torch.empty(x.rows, x.k, dtype=torch.bfloat16, device=dev)
+
+    def launch(self, fp4, stream):
+        fp4.fp4_mx_unpack(self.p, self.s, out=self.o, stream=stream)
+
+    def e2e_jobs(self, torch, fp4, chunks):
+        """[(h2d bytes, d2h bytes, fn(stream))] for row chunks, host buffers pinned."""
+        hp, hs = torch.from_numpy(self.x.packed).pin_memory(), torch.from_numpy(self.x.scales).pin_memory()
+        ho = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+        jobs = []
+        for r0, r1 in _row_chunks(self.x.rows, chunks):
+            def fn(st, r0=r0, r1=r1):
+                self.p[r0:r1].copy_(hp[r0:r1], non_blocking=True)
+                self.s[r0:r1].copy_(hs[r0:r1], non_blocking=True)
+                fp4.fp4_mx_unpack(self.p[r0:r1], self.s[r0:r1], out=self.o[r0:r1], stream=st)
+                ho[r0:r1].copy_(self.o[r0:r1], non_blocking=True)
+            jobs.append((hp[r0:r1].numel() + hs[r0:r1].numel(), ho[r0:r1].numel() * 2, fn))
+        return jobs
+
+    def oracle_units(self, o, n, threads):
+        o.mx_unpack(self.x.packed[:n], self.x.scales[:n], threads)
+
+    def sample_name(self):
+        return f"rows of {self.x.name}"
+
+
+class NvGatherOp:
+    """fp4_nv_embedding_gather of a batch of ids."""
+    kind, kernel = "nv_embedding_gather", "nv_gather_rows_kernel<true>"
+
+    def __init__(self, x):
+        self.x = x
+        self.elems = x.n_elems
+        self.bytes = x.algorithmic_bytes()
+        self.min_bytes = x.distinct_row_bytes()
+        self.units, self.elems_per_unit = x.ids.size, x.hidden
+
+    def to_device(self, torch, dev):
+        x = self.x
+        self.ids = torch.from_numpy(x.ids).to(dev)
+        self.w = torch.from_numpy(x.weight).to(dev)
+        self.sc = torch.from_numpy(x.scales).to(dev)
+        self.gs = torch.tensor([x.global_scale], dtype=torch.float32, device=dev)
+        self.o = torch.empty(*x.ids.shape, x.hidden, dtype=torch.bfloat16, device=dev)
+
+    def launch(self, fp4, stream):
+        fp4.fp4_nv_embedding_gather(self.ids, self.w, self.sc, self.gs, out=self.o, stream=stream)
+
+    def e2e_jobs(self, torch, fp4, chunks):
+        hi = torch.from_numpy(self.x.ids.reshape(-1)).pin_memory()
+        ids, o = self.ids.view(-1), self.o.view(-1, self.x.hidden)
+        ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+        jobs = []
+        for r0, r1 in _row_chunks(ids.shape[0], max(1, chunks // 2)):
+            def fn(st, r0=r0, r1=r1):
+                ids[r0:r1].copy_(hi[r0:r1], non_blocking=True)
+                fp4.fp4_nv_embedding_gather(ids[r0:r1], self.w, self.sc, self.gs, out=o[r0:r1],
+                                            stream=st)
+                ho[r0:r1].copy_(o[r0:r1], non_blocking=True)
+            jobs.append(((r1 - r0) * 8, ho[r0:r1].numel() * 2, fn))
+        return jobs
+
+    def oracle_units(self, o, n, threads):
+        x = self.x
+        o.nv_embedding_gather(x.ids.reshape(-1)[:n], x.weight, x.scales, x.global_scale,
+                              threads=threads)
+
+    def sample_name(self):
+        return f"ids of {self.x.name}"
+
+
+class NvDenseOp:
+    """fp4_nv_dequant of a whole table."""
+    kind, kernel = "nv_dequant", "nv_gather_rows_kernel<false>"
+
+    def __init__(self, x):
+        self.x = x
+        self.elems = x.vocab * x.hidden
+        self.bytes = x.vocab * (x.hidden // 2 + x.hidden // x.group_size + 2 * x.hidden)
+        self.min_bytes = self.bytes
+        self.units, self.elems_per_unit = x.vocab, x.hidden
+
+    def to_device(self, torch, dev):
+        x = self.x
+        self.w = torch.from_numpy(x.weight).to(dev)
+        self.sc = torch.from_numpy(x.scales).to(dev)
+        self.gs = torch.tensor([x.global_scale], dtype=torch.float32, device=dev)
+        self.o = torch.empty(x.vocab, x.hidden, dtype=torch.bfloat16, device=dev)
+
+    def launch(self, fp4, stream):
+        fp4.fp4_nv_dequant(self.w, self.sc, self.gs, out=self.o, stream=stream)
+
+    def e2e_jobs(self, torch, fp4, chunks):
+        hw, hs = torch.from_numpy(self.x.weight).pin_memory(), torch.from_numpy(self.x.scales).pin_memory()
+        ho = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+        jobs = []
+        for r0, r1 in _row_chunks(self.x.vocab, chunks):
+            def fn(st, r0=r0, r1=r1):
+                self.w[r0:r1].copy_(hw[r0:r1], non_blocking=True)
+                self.sc[r0:r1].copy_(hs[r0:r1], non_blocking=True)
+                fp4.fp4_nv_dequant(self.w[r0:r1], self.sc[r0:r1], self.gs, out=self.o[r0:r1],
+                                   stream=st)
+                ho[r0:r1].copy_(self.o[r0:r1], non_blocking=True)
+            jobs.append((hw[r0:r1].numel() + hs[r0:r1].numel(), ho[r0:r1].numel() * 2, fn))
+        return jobs
+
+    def oracle_units(self, o, n, threads):
+        x = self.x
+        o.nv_dequant(x.weight[:n], x.scales[:n], x.global_scale, threads=threads)
+
+    def sample_name(self):
+        return f"rows of the {self.x.name} table"
+
+
 def load_workload(name: str):
+    """The ops of one step of the named workload, in launch order."""
     from block_scaled_fp4_mx_gb300 import inputs
-    mx, nv = [], []
-    if name in ("step", "mx_moe"):
-        mx = inputs.mx_moe()
-    if name in ("step", "nv_embedding_200k"):
-        nv = [inputs.nv_embedding_200k()]
-    if name == "mx_stress":
-        mx = [inputs.mx_stress()]
-    if name == "mx_exhaustive":
-        mx = [inputs.mx_exhaustive()]
-    if name == "nv_embedding_32k":
-        nv = [inputs.nv_embedding_32k()]
-    return mx, nv
+    if name == "step":
+        return [MxOp(x) for x in inputs.mx_moe()] + [NvGatherOp(inputs.nv_embedding_200k())]
+    table = {
+        "mx_moe": lambda: [MxOp(x) for x in inputs.mx_moe()],
+        "mx_stress": lambda: [MxOp(inputs.mx_stress())],
+        "mx_exhaustive": lambda: [MxOp(inputs.mx_exhaustive())],
+        "nv_embedding_200k": lambda: [NvGatherOp(inputs.nv_embedding_200k())],
+        "nv_embedding_32k": lambda: [NvGatherOp(inputs.nv_embedding_32k())],
+        "nv_dequant_200k": lambda: [NvDenseOp(inputs.nv_embedding_200k())],
+        "nv_dequant_32k": lambda: [NvDenseOp(inputs.nv_embedding_32k())],
+    }
+    return table[name]()
 
 
-def workload_label(name: str, mx, nv) -> str:
+def workload_label(name: str) -> str:
     if name == "step":
         return ("mx_moe_unpack_32x(5760+2880)x2880 + "
                 "nv_embedding_gather_200000x8192_zipf1.1_ids64x256")
@@ -234,9 +366,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(elements_per_launch: float):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu capture,
-    scaled to this launch size; None when the kernel source changed since."""
+def ncu_traffic(kind: str, elements_per_launch: float):
+    """DRAM bytes per launch of the MXFP4 kernel from the committed ncu capture,
+    scaled to this launch size; None for other kernels or once the kernel source
+    changed since the capture."""
+    if kind != "mx_unpack":
+        return None, None
     path = os.path.join(ROOT, "profiles", "mx_unpack_dram_traffic.json")
     try:
         with open(path) as fh:
@@ -261,126 +396,105 @@ def run_ours(args, d: Dist):
     torch.cuda.set_device(dev)
     d.init("nccl")
     fp4.load()
-    mx_in, nv_in = load_workload(args.workload)
-
-    stream = torch.cuda.current_stream(dev)
-    mx_dev = [(torch.from_numpy(x.packed).to(dev), torch.from_numpy(x.scales).to(dev),
-               torch.empty(x.rows, x.k, dtype=torch.bfloat16, device=dev)) for x in mx_in]
-    nv_dev = [(torch.from_numpy(x.ids).to(dev), torch.from_numpy(x.weight).to(dev),
-               torch.from_numpy(x.scales).to(dev),
-               torch.tensor([x.global_scale], dtype=torch.float32, device=dev),
-               torch.empty(*x.ids.shape, x.hidden, dtype=torch.bfloat16, device=dev))
-              for x in nv_in]
+    ops = load_workload(args.workload)
+    for op in ops:
+        op.to_device(torch, dev)
     torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
 
-    mx_elems = sum(x.n_elems for x in mx_in)
-    nv_elems = sum(x.n_elems for x in nv_in)
-    step_elems = mx_elems + nv_elems
-    mx_bytes = sum(x.algorithmic_bytes() for x in mx_in)
-    nv_bytes = sum(x.algorithmic_bytes() for x in nv_in)
-    nv_min_bytes = sum(x.distinct_row_bytes() for x in nv_in)
-    launches_per_step = len(mx_in) + len(nv_in)
+    step_elems = sum(op.elems for op in ops)
+    step_bytes = sum(op.bytes for op in ops)
 
     def step(ev=None):
-        for i, (p, s, o) in enumerate(mx_dev):
+        for i, op in enumerate(ops):
             if ev is not None:
-                ev["mx"][i][0].record(stream)
-            fp4.fp4_mx_unpack(p, s, out=o, stream=stream)
+                ev[i][0].record(stream)
+            op.launch(fp4, stream)
             if ev is not None:
-                ev["mx"][i][1].record(stream)
-        for i, (ids, w, sc, gs, o) in enumerate(nv_dev):
-            if ev is not None:
-                ev["nv"][i][0].record(stream)
-            fp4.fp4_nv_embedding_gather(ids, w, sc, gs, out=o, stream=stream)
-            if ev is not None:
-                ev["nv"][i][1].record(stream)
+                ev[i][1].record(stream)
 
-    def new_events():
-        mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        return {"mx": [mk() for _ in mx_dev], "nv": [mk() for _ in nv_dev]}
-
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(dev.index)
     sampler.start()
-    per_step_events = [new_events() for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    events = [[mk() for _ in ops] for _ in range(args.steps)]
+    start, end = mk()
     d.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     start.record(stream)
     for k in range(args.steps):
-        step(per_step_events[k])
+        step(events[k])
     end.record(stream)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     d.barrier()
     sampler.stop()
-    elapsed_ms = start.elapsed_time(end)
-    elapsed_ms = d.max(elapsed_ms, dev)
-
-    mx_ms = sum(e[0].elapsed_time(e[1]) for ev in per_step_events for e in ev["mx"])
-    nv_ms = sum(e[0].elapsed_time(e[1]) for ev in per_step_events for e in ev["nv"])
+    elapsed_ms = d.max(start.elapsed_time(end), dev)
     k = args.steps
     value = step_elems * k * d.world / (elapsed_ms / 1e3)
-    alg_gbs = (mx_bytes + nv_bytes) * k / (elapsed_ms / 1e3) / 1e9
+    alg_gbs = step_bytes * k / (elapsed_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    clocks = sampler.summary(t0, t1)
 
+    # per kernel kind: summed bytes and durations of its launches
     kernels = {}
-    roofline = None
-    if mx_in:
-        mx_launch_s = mx_ms / 1e3 / (k * len(mx_in))
-        bytes_per_launch = mx_bytes / len(mx_in)
-        achieved = bytes_per_launch / mx_launch_s / 1e9
-        traffic, capture = ncu_traffic(mx_elems / len(mx_in))
-        kernels["mx_unpack"] = {"launches_per_step": len(mx_in), "avg_launch_us": mx_launch_s * 1e6,
-                                "elements_per_launch": mx_elems / len(mx_in),
-                                "algorithmic_bytes_per_launch": bytes_per_launch,
-                                "gbs": achieved, "frac_of_peak": achieved / peak}
-        roofline = {"kernel": "mx_unpack_words_kernel", "bound": "hbm", "achieved": achieved,
-                    "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if
-                    peak_kind == "measured" else "fallback 6.8 TB/s",
-                    "traffic": traffic,
-                    "traffic_source": capture}
-    if nv_in:
-        nv_launch_s = nv_ms / 1e3 / (k * len(nv_in))
-        kernels["nv_embedding_gather"] = {
-            "launches_per_step": len(nv_in), "avg_launch_us": nv_launch_s * 1e6,
-            "elements_per_launch": nv_elems / len(nv_in),
-            "logical_bytes_per_launch": nv_bytes / len(nv_in),
-            "distinct_row_bytes_per_launch": nv_min_bytes / len(nv_in),
-            "gbs_logical": nv_bytes / len(nv_in) / nv_launch_s / 1e9,
-            "gbs_distinct_rows": nv_min_bytes / len(nv_in) / nv_launch_s / 1e9,
-            "frac_of_peak_logical": nv_bytes / len(nv_in) / nv_launch_s / 1e9 / peak}
-        if roofline is None:
-            achieved = nv_bytes / len(nv_in) / nv_launch_s / 1e9
-            roofline = {"kernel": "nv_gather_rows_kernel", "bound": "hbm", "achieved": achieved,
-                        "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                        "peak_source": peak_kind, "traffic": None,
-                        "traffic_source": None}
+    for i, op in enumerate(ops):
+        ms = sum(ev[i][0].elapsed_time(ev[i][1]) for ev in events)
+        kk = kernels.setdefault(op.kind, {"kernel": op.kernel, "launches_per_step": 0, "ms": 0.0,
+                                          "elements": 0, "bytes": 0, "min_bytes": 0})
+        kk["launches_per_step"] += 1
+        kk["ms"] += ms
+        kk["elements"] += op.elems
+        kk["bytes"] += op.bytes
+        kk["min_bytes"] += op.min_bytes
+    for kk in kernels.values():
+        n = kk["launches_per_step"]
+        launch_s = kk.pop("ms") / 1e3 / (k * n)
+        kk.update(avg_launch_us=launch_s * 1e6, elements_per_launch=kk["elements"] / n,
+                  algorithmic_bytes_per_launch=kk["bytes"] / n,
+                  gbs=kk["bytes"] / n / launch_s / 1e9,
+                  frac_of_peak=kk["bytes"] / n / launch_s / 1e9 / peak)
+        if kk["min_bytes"] != kk["bytes"]:
+            kk["distinct_row_bytes_per_launch"] = kk["min_bytes"] / n
+            kk["gbs_distinct_rows"] = kk["min_bytes"] / n / launch_s / 1e9
+        for key in ("elements", "bytes", "min_bytes"):
+            kk.pop(key)
+    dominant = max(kernels, key=lambda kind: kernels[kind]["avg_launch_us"]
+                   * kernels[kind]["launches_per_step"])
+    dk = kernels[dominant]
+    traffic, capture = ncu_traffic(dominant, dk["elements_per_launch"])
+    roofline = {"kernel": dk["kernel"], "bound": "hbm", "achieved": dk["gbs"], "peak": peak,
+                "unit": "GB/s", "frac": dk["gbs"] / peak,
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "traffic": traffic, "traffic_source": capture}
 
-    e2e = None if args.no_e2e else run_e2e(args, d, dev, mx_in, nv_in, mx_dev, nv_dev, step_elems)
+    e2e = None if args.no_e2e else run_e2e(args, d, dev, ops, step_elems)
     cpu = None
     if d.rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(mx_in, nv_in, budget_s=args.cpu_budget)
+        cpu = cpu_baseline(ops, budget_s=args.cpu_budget)
 
+    in_bytes = sum(op.bytes - 2 * op.elems for op in ops)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": d.world, "steps": k,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / k, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int16+fp32", "data": "synthetic",
-        "config": {"workload": workload_label(args.workload, mx_in, nv_in),
-                   "mx_elements_per_step": mx_elems, "nv_elements_per_step": nv_elems,
-                   "algorithmic_bytes_per_step": mx_bytes + nv_bytes,
-                   "l2": "inputs (398 MB packed MoE codes, 922 MB packed table) and outputs "
-                         "(1.86 GB) larger than the 129 MB L2; no flush",
+        "config": {"workload": workload_label(args.workload),
+                   "elements_per_step": step_elems,
+                   "elements_per_step_by_kernel": {
+                       kind: sum(op.elems for op in ops if op.kind == kind)
+                       for kind in dict.fromkeys(op.kind for op in ops)},
+                   "algorithmic_bytes_per_step": step_bytes,
+                   "l2": ("no flush: inputs (%.0f MB) and outputs (%.0f MB) per step exceed the "
+                          "129 MB L2" % (in_bytes / 1e6, 2 * step_elems / 1e6))
+                   if step_bytes > 4 * 129e6 else "no flush: working set smaller than L2",
                    "parallelism": f"replicas x{d.world}"},
         "hbm_gbs_algorithmic": alg_gbs, "pct_of_peak_hbm": 100.0 * alg_gbs / peak,
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches_per_step * k, "clocks": clocks,
+        "gpu_launches": len(ops) * k, "clocks": sampler.summary(t0, t1),
         "device": torch.cuda.get_device_name(dev),
     }
     if d.rank == 0:
@@ -393,7 +507,7 @@ def _row_chunks(n: int, chunks: int):
     return [(r, min(n, r + step)) for r in range(0, n, step)]
 
 
-def run_e2e(args, d, dev, mx_in, nv_in, mx_dev, nv_dev, step_elems):
+def run_e2e(args, d, dev, ops, step_elems):
     """Same steps through the public API with pinned host buffers: every step
     copies its inputs host->device, decodes, and copies its outputs back. Each
     tensor is cut into row chunks issued round-robin on a few streams, so the
@@ -405,42 +519,19 @@ def run_e2e(args, d, dev, mx_in, nv_in, mx_dev, nv_dev, step_elems):
 
     main = torch.cuda.current_stream(dev)
     streams = [torch.cuda.Stream(dev) for _ in range(max(1, args.e2e_streams))]
-    pin = lambda a: torch.from_numpy(a).pin_memory()
-    mx_host = [(pin(x.packed), pin(x.scales),
-                torch.empty(x.rows, x.k, dtype=torch.bfloat16).pin_memory()) for x in mx_in]
-    nv_host = [(pin(x.ids.reshape(-1)),
-                torch.empty(x.ids.size, x.hidden, dtype=torch.bfloat16).pin_memory())
-               for x in nv_in]
-    nv_flat = [(ids.view(-1), w, sc, gs, o.view(-1, o.shape[-1])) for ids, w, sc, gs, o in nv_dev]
-    h2d = sum(p.numel() + s.numel() for p, s, _ in mx_host) + sum(i.numel() * 8 for i, _ in nv_host)
-    d2h = sum(o.numel() * 2 for *_, o in mx_host) + sum(o.numel() * 2 for _, o in nv_host)
-    jobs = []
-    for (hp, hs, ho), (p, s, o) in zip(mx_host, mx_dev):
-        for r0, r1 in _row_chunks(p.shape[0], args.e2e_chunks):
-            jobs.append(("mx", (hp[r0:r1], hs[r0:r1], ho[r0:r1]), (p[r0:r1], s[r0:r1], o[r0:r1])))
-    for (hi, ho), (ids, w, sc, gs, o) in zip(nv_host, nv_flat):
-        for r0, r1 in _row_chunks(ids.shape[0], max(1, args.e2e_chunks // 2)):
-            jobs.append(("nv", (hi[r0:r1], ho[r0:r1]), (ids[r0:r1], w, sc, gs, o[r0:r1])))
+    jobs = [j for op in ops for j in op.e2e_jobs(torch, fp4, args.e2e_chunks)]
+    h2d = sum(j[0] for j in jobs)
+    d2h = sum(j[1] for j in jobs)
 
     def step():
         start = torch.cuda.Event()
         start.record(main)
         for st in streams:
             st.wait_event(start)
-        for j, (kind, host, devb) in enumerate(jobs):
-            st = streams[j % len(streams)]
+        for n, (_, _, fn) in enumerate(jobs):
+            st = streams[n % len(streams)]
             with torch.cuda.stream(st):
-                if kind == "mx":
-                    (hp, hs, ho), (p, s, o) = host, devb
-                    p.copy_(hp, non_blocking=True)
-                    s.copy_(hs, non_blocking=True)
-                    fp4.fp4_mx_unpack(p, s, out=o, stream=st)
-                    ho.copy_(o, non_blocking=True)
-                else:
-                    (hi, ho), (ids, w, sc, gs, o) = host, devb
-                    ids.copy_(hi, non_blocking=True)
-                    fp4.fp4_nv_embedding_gather(ids, w, sc, gs, out=o, stream=st)
-                    ho.copy_(o, non_blocking=True)
+                fn(st)
         for st in streams:
             done = torch.cuda.Event()
             done.record(st)
@@ -464,83 +555,53 @@ def run_e2e(args, d, dev, mx_in, nv_in, mx_dev, nv_dev, step_elems):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps, "gpu_launches_per_step": len(jobs),
             "host_link_gbs": (h2d + d2h) / (ms / steps / 1e3) / 1e9,
-            "note": f"MXFP4 codes+scales and token ids copied in, all bf16 outputs copied out, "
-                    f"{len(jobs)} row chunks on {len(streams)} streams; the NVFP4 table stays "
-                    f"resident (model weights)"}
+            "note": f"each step's packed codes, scales and ids copied in and all bf16 outputs "
+                    f"copied out, {len(jobs)} row chunks on {len(streams)} streams; an "
+                    f"embedding table being gathered from stays resident (model weights)"}
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle timings
 # ---------------------------------------------------------------------------
 
-def _mx_sample(x, rows):
-    return x.packed[:rows], x.scales[:rows]
-
-
-def cpu_rates(mx_in, nv_in, seconds: float):
-    """Oracle throughput (elements/s) on leading slices of the workload, sized to
-    take about ``seconds`` each; returns (mx_rate, nv_rate, description, threads)."""
-    import numpy as np
-
+def cpu_rates(ops, seconds: float):
+    """Oracle throughput (elements/s) per op kind, on leading units (rows or ids)
+    of the first op of that kind, sized to take about ``seconds`` each.
+    Returns ({kind: (rate, units)}, description, threads)."""
     import oracle
 
     o = oracle.get()
     threads = o.max_threads()
-    desc = []
-    mx_rate = nv_rate = None
-    if mx_in:
-        x = mx_in[0]
-        rows = max(1, min(x.rows, 64))
+    rates, desc = {}, []
+    for kind in dict.fromkeys(op.kind for op in ops):
+        op = next(p for p in ops if p.kind == kind)
+        n = max(1, min(op.units, 16))
         while True:
-            p, s = _mx_sample(x, rows)
             t = time.perf_counter()
-            o.mx_unpack(p, s, threads)
+            op.oracle_units(o, n, threads)
             dt = time.perf_counter() - t
-            if dt >= seconds / 4 or rows == x.rows:
+            if dt >= seconds / 4 or n == op.units:
                 break
-            rows = min(x.rows, int(rows * max(2.0, seconds / 2 / max(dt, 1e-4))))
+            n = min(op.units, int(n * max(2.0, seconds / 2 / max(dt, 1e-4))))
         reps, total = 0, 0.0
         while total < seconds and reps < 50:
             t = time.perf_counter()
-            o.mx_unpack(p, s, threads)
+            op.oracle_units(o, n, threads)
             total += time.perf_counter() - t
             reps += 1
-        mx_rate = rows * x.k * reps / total
-        desc.append(f"MXFP4: first {rows} rows of {x.name} ({rows * x.k} codes) x{reps}")
-    if nv_in:
-        x = nv_in[0]
-        flat = x.ids.reshape(-1)
-        n = max(1, min(flat.size, 16))
-        while True:
-            t = time.perf_counter()
-            o.nv_embedding_gather(flat[:n], x.weight, x.scales, x.global_scale, threads=threads)
-            dt = time.perf_counter() - t
-            if dt >= seconds / 4 or n == flat.size:
-                break
-            n = min(flat.size, int(n * max(2.0, seconds / 2 / max(dt, 1e-4))))
-        reps, total = 0, 0.0
-        while total < seconds and reps < 50:
-            t = time.perf_counter()
-            o.nv_embedding_gather(flat[:n], x.weight, x.scales, x.global_scale, threads=threads)
-            total += time.perf_counter() - t
-            reps += 1
-        nv_rate = n * x.hidden * reps / total
-        desc.append(f"NVFP4: first {n} ids of {x.name} ({n * x.hidden} codes) x{reps}")
-    return mx_rate, nv_rate, "; ".join(desc), threads
+        rates[kind] = (n * op.elems_per_unit * reps / total, n)
+        desc.append(f"{kind}: first {n} {op.sample_name()} ({n * op.elems_per_unit} codes) x{reps}")
+    return rates, "; ".join(desc), threads
 
 
-def cpu_baseline(mx_in, nv_in, budget_s: float = 10.0) -> dict:
-    parts = (1 if mx_in else 0) + (1 if nv_in else 0)
-    mx_rate, nv_rate, desc, threads = cpu_rates(mx_in, nv_in, budget_s / max(1, parts))
-    t_step = 0.0
-    if mx_in:
-        t_step += sum(x.n_elems for x in mx_in) / mx_rate
-    if nv_in:
-        t_step += sum(x.n_elems for x in nv_in) / nv_rate
-    total = sum(x.n_elems for x in mx_in) + sum(x.n_elems for x in nv_in)
+def cpu_baseline(ops, budget_s: float = 10.0) -> dict:
+    kinds = list(dict.fromkeys(op.kind for op in ops))
+    rates, desc, threads = cpu_rates(ops, budget_s / max(1, len(kinds)))
+    t_step = sum(op.elems / rates[op.kind][0] for op in ops)
+    total = sum(op.elems for op in ops)
     return {"value": total / t_step, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": desc + "; rates combined in the step's element mix",
-            "mx_elements_per_s": mx_rate, "nv_elements_per_s": nv_rate,
+            "elements_per_s_by_kernel": {kind: rates[kind][0] for kind in kinds},
             "cpu": _cpu_model()}
 
 
@@ -562,31 +623,26 @@ def run_reference(args, d: Dist):
     import oracle
 
     oracle.build()
-    mx_in, nv_in = load_workload(args.workload)
+    ops = load_workload(args.workload)
+    kinds = list(dict.fromkeys(op.kind for op in ops))
     per_step = max(0.5, min(20.0, args.reference_budget / max(1, args.steps + args.warmup)))
-    mx_rate, nv_rate, desc, threads = cpu_rates(mx_in, nv_in, per_step / 2)
-    # each step: the sampled slices once, timed
+    rates, desc, threads = cpu_rates(ops, per_step / len(kinds))
     o = oracle.get()
+    # each step: one leading slice per op kind, sized to about per_step / kinds seconds
+    plan = []
+    for kind in kinds:
+        op = next(p for p in ops if p.kind == kind)
+        n = max(1, min(op.units, int(rates[kind][0] * per_step / len(kinds) / op.elems_per_unit)))
+        plan.append((op, n))
+    sample_elems = sum(n * op.elems_per_unit for op, n in plan)
     times = []
-    sample_elems = 0
     for i in range(args.warmup + args.steps):
         t = time.perf_counter()
-        elems = 0
-        if mx_in:
-            x = mx_in[0]
-            rows = max(1, min(x.rows, int(mx_rate * per_step / 2 / x.k)))
-            o.mx_unpack(x.packed[:rows], x.scales[:rows], threads)
-            elems += rows * x.k
-        if nv_in:
-            x = nv_in[0]
-            n = max(1, min(x.ids.size, int(nv_rate * per_step / 2 / x.hidden)))
-            o.nv_embedding_gather(x.ids.reshape(-1)[:n], x.weight, x.scales, x.global_scale,
-                                  threads=threads)
-            elems += n * x.hidden
+        for op, n in plan:
+            op.oracle_units(o, n, threads)
         dt = time.perf_counter() - t
         if i >= args.warmup:
             times.append(dt)
-            sample_elems = elems
     sec = sum(times)
     value = sample_elems * len(times) / sec
     line = {
@@ -594,10 +650,12 @@ def run_reference(args, d: Dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int16+fp32",
         "data": "synthetic",
-        "config": {"workload": workload_label(args.workload, mx_in, nv_in),
+        "config": {"workload": workload_label(args.workload),
                    "parallelism": "rank 0 only (CPU)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"per step {sample_elems} codes: {desc}", "cpu": _cpu_model()},
+                         "sample": "per step " + ", ".join(
+                             f"{n} {op.sample_name()} ({n * op.elems_per_unit} codes)"
+                             for op, n in plan), "cpu": _cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     emit(line, args)
@@ -621,7 +679,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--e2e-chunks", type=int, default=8,
-                    help="row chunks per MXFP4 tensor in the e2e leg (half as many for NVFP4)")
+                    help="row chunks per tensor in the e2e leg (half as many for a gather)")
     ap.add_argument("--e2e-streams", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

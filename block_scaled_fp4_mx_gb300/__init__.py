@@ -16,12 +16,15 @@ status raise.
   embedding lookup dequantised at gather time: value * (e4m3 block scale * fp32
   global scale) in fp32, rounded to bf16 ("sgl-project/sglang pull 34222",
   "Implementation breakdown", "Key source snippets").
+* ``fp4_nv_dequant(weight, block_scale, global_scale)`` -- the same NVFP4 decode
+  over every row of a table (e.g. a tied lm_head; same page, "Comments", "Risks").
 """
 from __future__ import annotations
 
 from ._lib import Status, last_error, library_path, load, status_string  # noqa: F401
 
-__all__ = ["fp4_mx_unpack", "fp4_nv_embedding_gather", "fp4_status_string", "Fp4Error",
+__all__ = ["fp4_mx_unpack", "fp4_nv_embedding_gather", "fp4_nv_dequant", "fp4_status_string",
+           "Fp4Error",
            "Status", "load", "library_path"]
 
 
@@ -139,4 +142,38 @@ def fp4_nv_embedding_gather(ids, weight, block_scale, global_scale, group_size: 
         _stream_handle(stream, weight.device))
     if code != Status.OK:
         raise Fp4Error("fp4_nv_embedding_gather", code)
+    return out
+
+
+def fp4_nv_dequant(weight, block_scale, global_scale, group_size: int = 16, out=None,
+                   stream=None):
+    """Dequantise a whole NVFP4 table -> bf16 [rows, hidden]: row r is what
+    fp4_nv_embedding_gather writes for id r. ``weight`` uint8 [rows, hidden/2],
+    ``block_scale`` float8_e4m3fn (or uint8 bits) [rows, hidden/16], ``global_scale``
+    fp32 CUDA tensor with one element."""
+    torch = _torch()
+    _check_cuda(weight, "weight", (torch.uint8,))
+    _check_cuda(block_scale, "block_scale", (torch.float8_e4m3fn, torch.uint8))
+    _check_cuda(global_scale, "global_scale", (torch.float32,))
+    if global_scale.numel() != 1:
+        raise ValueError("global_scale must have exactly one element")
+    if weight.dim() != 2 or block_scale.dim() != 2:
+        raise ValueError("weight and block_scale must be 2-D [rows, ...]")
+    rows, half = weight.shape
+    hidden = 2 * half
+    if block_scale.shape[0] != rows:
+        raise ValueError("weight and block_scale have different row counts")
+    if group_size > 0 and hidden % group_size == 0 and block_scale.shape[1] * group_size != hidden:
+        raise ValueError(f"block_scale must be [rows, hidden/{group_size}]")
+    if out is None:
+        out = torch.empty((rows, hidden), dtype=torch.bfloat16, device=weight.device)
+    else:
+        _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
+        if tuple(out.shape) != (rows, hidden):
+            raise ValueError(f"out must have shape {(rows, hidden)}")
+    code = load().fp4_nv_dequant(_ptr(weight), _ptr(block_scale), _ptr(global_scale), rows,
+                                 hidden, int(group_size), _ptr(out),
+                                 _stream_handle(stream, weight.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_nv_dequant", code)
     return out

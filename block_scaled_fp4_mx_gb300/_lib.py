@@ -36,6 +36,7 @@ SIGNATURES = {
     "fp4_mx_unpack": ([_vp, _vp, _vp, _i64, _i64, _vp], ctypes.c_int),
     "fp4_nv_embedding_gather": ([_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp],
                                 ctypes.c_int),
+    "fp4_nv_dequant": ([_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp], ctypes.c_int),
     "fp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "fp4_last_error": ([], ctypes.c_char_p),
     "fp4_abi_version": ([], ctypes.c_int),

@@ -161,6 +161,32 @@ FP4_EXPORT fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_id
     return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_nv_embedding_gather launch");
 }
 
+FP4_EXPORT fp4_status fp4_nv_dequant(const uint8_t *weight, const uint8_t *block_scale_e4m3,
+                                     const float *global_scale, int64_t rows, int64_t hidden,
+                                     int64_t group_size, uint16_t *out_bf16,
+                                     fp4_stream_t stream) {
+    clear_error();
+    if (rows < 0 || hidden <= 0 || group_size <= 0) return FP4_ERR_SHAPE;
+    if (hidden % group_size != 0) return FP4_ERR_GROUP;
+    if (group_size != 16) return FP4_ERR_UNSUPPORTED;
+    if (rows == 0) return FP4_OK;
+    if (rows > INT64_MAX / 2 / hidden) return FP4_ERR_SHAPE;
+    if (weight == nullptr || block_scale_e4m3 == nullptr || global_scale == nullptr ||
+        out_bf16 == nullptr)
+        return FP4_ERR_NULL_PTR;
+    const uint64_t out_bytes = (uint64_t)rows * (uint64_t)hidden * 2;
+    if (overlaps(out_bf16, out_bytes, weight, (uint64_t)rows * (uint64_t)hidden / 2) ||
+        overlaps(out_bf16, out_bytes, block_scale_e4m3, (uint64_t)rows * (uint64_t)hidden / 16) ||
+        overlaps(out_bf16, out_bytes, global_scale, 4))
+        return FP4_ERR_ALIAS;
+    const void *ptrs[] = {weight, block_scale_e4m3, global_scale, out_bf16};
+    const fp4_status s = check_pointers(ptrs, 4);
+    if (s != FP4_OK) return s;
+    const cudaError_t err = fp4mx::launch_nv_dequant(weight, block_scale_e4m3, global_scale, rows,
+                                                     hidden, out_bf16, (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_nv_dequant launch");
+}
+
 FP4_EXPORT const char *fp4_status_string(fp4_status status) {
     switch (status) {
     case FP4_OK: return "ok";
@@ -178,4 +204,4 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 100; }
+FP4_EXPORT int fp4_abi_version(void) { return 101; }

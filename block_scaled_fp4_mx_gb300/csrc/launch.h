@@ -19,6 +19,11 @@ cudaError_t launch_nv_gather(const int64_t *ids, int64_t num_ids, const uint8_t 
                              int64_t hidden, uint16_t *out, int32_t *err_flag,
                              cudaStream_t stream);
 
+// Dequantise every row of a [rows, hidden] NVFP4 table (rows > 0).
+cudaError_t launch_nv_dequant(const uint8_t *weight, const uint8_t *scales,
+                              const float *global_scale, int64_t rows, int64_t hidden,
+                              uint16_t *out, cudaStream_t stream);
+
 // Resident CTAs per SM x SM count for `kernel` at `threads` threads, cached per
 // device; a grid no larger than this runs in one wave.
 int max_resident_ctas(const void *kernel, int threads, int slot);

@@ -29,18 +29,21 @@ constexpr uint32_t kSegWords = 32 * kUnroll;
 
 // Warp per (row, segment). Rows are [0, num_rows) of this launch; unit = row *
 // segs_per_row + segment fits in 32 bits (the launcher splits larger calls).
+// kGather: the source row is ids[t] (embedding lookup); otherwise it is
+// row0 + t (dense dequant of a table, ids unused).
+template <bool kGather>
 __global__ void __launch_bounds__(kThreads)
 nv_gather_rows_kernel(const int64_t *__restrict__ ids, uint32_t n_units,
                       const uint32_t *__restrict__ weight, const uint8_t *__restrict__ scales,
                       const float *__restrict__ global_scale, int64_t vocab,
                       uint32_t words_per_row, uint32_t segs_per_row, uint4 *__restrict__ out,
-                      int32_t *__restrict__ err_flag) {
+                      int32_t *__restrict__ err_flag, int64_t row0) {
     const uint32_t unit = blockIdx.x * (uint32_t)kWarps + (threadIdx.x >> 5);
     if (unit >= n_units) return;
     const int lane = threadIdx.x & 31;
     const uint32_t t = unit / segs_per_row;
     const uint32_t w0 = (unit - t * segs_per_row) * kSegWords;
-    const int64_t id = __ldg(ids + t);
+    const int64_t id = kGather ? __ldg(ids + t) : row0 + t;
     uint4 *out_row = out + (int64_t)t * words_per_row;
     if (id < 0 || id >= vocab) {
 #pragma unroll
@@ -73,12 +76,13 @@ nv_gather_rows_kernel(const int64_t *__restrict__ ids, uint32_t n_units,
 
 // Thread per word of the flattened [num_rows, words_per_row] output, kUnroll
 // words per thread strided by kThreads (for rows narrower than a warp's loads).
+template <bool kGather>
 __global__ void __launch_bounds__(kThreads)
 nv_gather_flat_kernel(const int64_t *__restrict__ ids, int64_t n_words,
                       const uint32_t *__restrict__ weight, const uint8_t *__restrict__ scales,
                       const float *__restrict__ global_scale, int64_t vocab,
                       uint32_t words_per_row, uint4 *__restrict__ out,
-                      int32_t *__restrict__ err_flag) {
+                      int32_t *__restrict__ err_flag, int64_t row0) {
     const int64_t base = (int64_t)blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
     const float gs = __ldg(global_scale);
 #pragma unroll
@@ -87,7 +91,7 @@ nv_gather_flat_kernel(const int64_t *__restrict__ ids, int64_t n_words,
         if (f >= n_words) continue;
         const int64_t t = f / words_per_row;
         const uint32_t i = (uint32_t)(f - t * words_per_row);
-        const int64_t id = __ldg(ids + t);
+        const int64_t id = kGather ? __ldg(ids + t) : row0 + t;
         if (id < 0 || id >= vocab) {
             st_stream(out + f, make_uint4(0, 0, 0, 0));
             if (i == 0 && err_flag != nullptr) atomicExch(err_flag, FP4_ERR_INDEX);
@@ -100,6 +104,7 @@ nv_gather_flat_kernel(const int64_t *__restrict__ ids, int64_t n_words,
 }
 
 // Any alignment: one thread per packed byte of the output (two codes).
+template <bool kGather>
 __global__ void __launch_bounds__(kThreads)
 nv_gather_bytes_kernel(const int64_t *__restrict__ ids, int64_t num_ids,
                        const uint8_t *__restrict__ weight, const uint8_t *__restrict__ scales,
@@ -113,7 +118,7 @@ nv_gather_bytes_kernel(const int64_t *__restrict__ ids, int64_t num_ids,
          i += (int64_t)gridDim.x * kThreads) {
         const int64_t t = i / half;
         const int64_t b = i - t * half;
-        const int64_t id = ids[t];
+        const int64_t id = kGather ? ids[t] : t;
         uint16_t *o = out + t * hidden + 2 * b;
         if (id < 0 || id >= vocab) {
             o[0] = 0;
@@ -128,50 +133,80 @@ nv_gather_bytes_kernel(const int64_t *__restrict__ ids, int64_t num_ids,
     }
 }
 
+// Vectorised path shared by the gather and the dense dequant: row-segment
+// kernel for rows of at least 32 words, flat kernel below that.
+template <bool kGather>
+void launch_nv_words(const int64_t *ids, int64_t num_rows, const uint8_t *weight,
+                     const uint8_t *scales, const float *global_scale, int64_t vocab,
+                     int64_t hidden, uint16_t *out, int32_t *err_flag, cudaStream_t stream) {
+    const int64_t words_per_row = hidden / 8;
+    if (words_per_row >= 32) {
+        // rows in pieces so that row * segments stays below 2^31
+        const int64_t segs = (words_per_row + kSegWords - 1) / kSegWords;
+        const int64_t rows_per_launch = ((int64_t)1 << 31) / segs;
+        for (int64_t r0 = 0; r0 < num_rows; r0 += rows_per_launch) {
+            const int64_t rows = num_rows - r0 < rows_per_launch ? num_rows - r0 : rows_per_launch;
+            const int64_t units = rows * segs;
+            const int grid = (int)((units + kWarps - 1) / kWarps);
+            nv_gather_rows_kernel<kGather><<<grid, kThreads, 0, stream>>>(
+                kGather ? ids + r0 : nullptr, (uint32_t)units,
+                reinterpret_cast<const uint32_t *>(weight), scales, global_scale, vocab,
+                (uint32_t)words_per_row, (uint32_t)segs,
+                reinterpret_cast<uint4 *>(out) + r0 * words_per_row, err_flag, r0);
+        }
+    } else {
+        constexpr int64_t kChunk = (int64_t)kThreads * kUnroll;
+        const int64_t rows_per_launch = ((int64_t)1 << 40) / words_per_row;
+        for (int64_t r0 = 0; r0 < num_rows; r0 += rows_per_launch) {
+            const int64_t rows = num_rows - r0 < rows_per_launch ? num_rows - r0 : rows_per_launch;
+            const int64_t n_words = rows * words_per_row;
+            const int grid = (int)((n_words + kChunk - 1) / kChunk);
+            nv_gather_flat_kernel<kGather><<<grid, kThreads, 0, stream>>>(
+                kGather ? ids + r0 : nullptr, n_words, reinterpret_cast<const uint32_t *>(weight),
+                scales, global_scale, vocab, (uint32_t)words_per_row,
+                reinterpret_cast<uint4 *>(out) + r0 * words_per_row, err_flag, r0);
+        }
+    }
+}
+
+bool vectorisable(const uint8_t *weight, const uint16_t *out) {
+    return (reinterpret_cast<uintptr_t>(weight) % 4 == 0) &&
+           (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+}
+
 }  // namespace
 
 cudaError_t launch_nv_gather(const int64_t *ids, int64_t num_ids, const uint8_t *weight,
                              const uint8_t *scales, const float *global_scale, int64_t vocab,
                              int64_t hidden, uint16_t *out, int32_t *err_flag,
                              cudaStream_t stream) {
-    const bool vector_ok = (reinterpret_cast<uintptr_t>(weight) % 4 == 0) &&
-                           (reinterpret_cast<uintptr_t>(out) % 16 == 0);
-    if (vector_ok) {
-        const int64_t words_per_row = hidden / 8;
-        if (words_per_row >= 32) {
-            // rows in pieces so that row * segments stays below 2^31
-            const int64_t segs = (words_per_row + kSegWords - 1) / kSegWords;
-            const int64_t rows_per_launch = ((int64_t)1 << 31) / segs;
-            for (int64_t r0 = 0; r0 < num_ids; r0 += rows_per_launch) {
-                const int64_t rows = num_ids - r0 < rows_per_launch ? num_ids - r0 : rows_per_launch;
-                const int64_t units = rows * segs;
-                const int grid = (int)((units + kWarps - 1) / kWarps);
-                nv_gather_rows_kernel<<<grid, kThreads, 0, stream>>>(
-                    ids + r0, (uint32_t)units, reinterpret_cast<const uint32_t *>(weight), scales,
-                    global_scale, vocab, (uint32_t)words_per_row, (uint32_t)segs,
-                    reinterpret_cast<uint4 *>(out) + r0 * words_per_row, err_flag);
-            }
-        } else {
-            constexpr int64_t kChunk = (int64_t)kThreads * kUnroll;
-            const int64_t rows_per_launch = ((int64_t)1 << 40) / words_per_row;
-            for (int64_t r0 = 0; r0 < num_ids; r0 += rows_per_launch) {
-                const int64_t rows = num_ids - r0 < rows_per_launch ? num_ids - r0 : rows_per_launch;
-                const int64_t n_words = rows * words_per_row;
-                const int grid = (int)((n_words + kChunk - 1) / kChunk);
-                nv_gather_flat_kernel<<<grid, kThreads, 0, stream>>>(
-                    ids + r0, n_words, reinterpret_cast<const uint32_t *>(weight), scales,
-                    global_scale, vocab, (uint32_t)words_per_row,
-                    reinterpret_cast<uint4 *>(out) + r0 * words_per_row, err_flag);
-            }
-        }
+    if (vectorisable(weight, out)) {
+        launch_nv_words<true>(ids, num_ids, weight, scales, global_scale, vocab, hidden, out,
+                              err_flag, stream);
     } else {
         const int64_t n = num_ids * (hidden / 2);
         const int64_t blocks = (n + kThreads - 1) / kThreads;
-        const int cap = max_resident_ctas((const void *)nv_gather_bytes_kernel, kThreads, 3);
+        const int cap = max_resident_ctas((const void *)nv_gather_bytes_kernel<true>, kThreads, 3);
         const int grid = (int)(blocks < cap ? blocks : cap);
-        nv_gather_bytes_kernel<<<grid, kThreads, 0, stream>>>(ids, num_ids, weight, scales,
-                                                              global_scale, vocab, hidden, out,
-                                                              err_flag);
+        nv_gather_bytes_kernel<true><<<grid, kThreads, 0, stream>>>(
+            ids, num_ids, weight, scales, global_scale, vocab, hidden, out, err_flag);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nv_dequant(const uint8_t *weight, const uint8_t *scales,
+                              const float *global_scale, int64_t rows, int64_t hidden,
+                              uint16_t *out, cudaStream_t stream) {
+    if (vectorisable(weight, out)) {
+        launch_nv_words<false>(nullptr, rows, weight, scales, global_scale, rows, hidden, out,
+                               nullptr, stream);
+    } else {
+        const int64_t n = rows * (hidden / 2);
+        const int64_t blocks = (n + kThreads - 1) / kThreads;
+        const int cap = max_resident_ctas((const void *)nv_gather_bytes_kernel<false>, kThreads, 4);
+        const int grid = (int)(blocks < cap ? blocks : cap);
+        nv_gather_bytes_kernel<false><<<grid, kThreads, 0, stream>>>(
+            nullptr, rows, weight, scales, global_scale, rows, hidden, out, nullptr);
     }
     return cudaGetLastError();
 }

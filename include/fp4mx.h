@@ -2,7 +2,7 @@
  * fp4mx.h -- C ABI of a GB300 (sm_103a) library that decodes block-scaled FP4
  * (E2M1) data into bf16.
  *
- * Two operations, each one CUDA kernel launch on the caller's stream:
+ * Three operations, each one CUDA kernel launch on the caller's stream:
  *
  *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
  *                             a wrapping 16-bit integer add into the bf16 exponent
@@ -11,6 +11,7 @@
  *                             codes and of e4m3 scales (one per 16 codes); each
  *                             value is multiplied by (block scale * global scale)
  *                             in fp32 and rounded to bf16 (nearest, ties to even).
+ *   fp4_nv_dequant            the same NVFP4 decode over every row of a table.
  *
  * Conventions shared by every entry point:
  *   - Pointers named "device" must be device-accessible CUDA allocations
@@ -118,6 +119,29 @@ fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_ids, const ui
                                    int64_t vocab, int64_t hidden, int64_t group_size,
                                    uint16_t *out_bf16, int32_t *err_flag, fp4_stream_t stream);
 
+/*
+ * fp4_nv_dequant -- dequantise a whole NVFP4 table (every row, in order).
+ *
+ * The dense counterpart of fp4_nv_embedding_gather: out[r][c] is what the
+ * gather writes for id = r. "sgl-project/sglang pull 34222" (prhub digest),
+ * sections "Comments" and "Risks": with tied word embeddings the lm_head is the
+ * embedding table, and the gather-only method's apply() cannot serve it; the
+ * table dequantised to bf16 is what that use needs. Same element rule, op order
+ * and rounding as the gather (see above).
+ *
+ *   weight           device, uint8[rows * hidden / 2], row-major [rows, hidden/2]
+ *   block_scale_e4m3 device, uint8[rows * hidden / 16] e4m3fn bits, [rows, hidden/16]
+ *   global_scale     device, one fp32
+ *   rows             >= 0 (0: nothing is launched)
+ *   hidden           > 0, hidden % group_size == 0 (else FP4_ERR_GROUP)
+ *   group_size       must be 16; other positive values: FP4_ERR_UNSUPPORTED
+ *   out_bf16         device, uint16[rows * hidden], row-major [rows, hidden]
+ *   stream           CUDA stream the kernel is enqueued on
+ */
+fp4_status fp4_nv_dequant(const uint8_t *weight, const uint8_t *block_scale_e4m3,
+                          const float *global_scale, int64_t rows, int64_t hidden,
+                          int64_t group_size, uint16_t *out_bf16, fp4_stream_t stream);
+
 /* Static English text for a status code ("unknown status" for other values). */
 const char *fp4_status_string(fp4_status status);
 
@@ -125,7 +149,7 @@ const char *fp4_status_string(fp4_status status);
  * until this thread's next call into the library. */
 const char *fp4_last_error(void);
 
-/* Version of this ABI (major * 100 + minor). */
+/* Version of this ABI (major * 100 + minor): 101 adds fp4_nv_dequant. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

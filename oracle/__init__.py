@@ -15,6 +15,8 @@ Functions and the passages they follow (web pages cited by title and section):
 * ``e4m3_to_f32``, ``f32_to_bf16_rne``, ``e2m1_bf16_bits`` -- the element
   conversions those steps use (OCP FP8 E4M3 definition; IEEE round to nearest
   even into bf16; the E2M1 codebook).
+* ``nv_dequant`` -- the same NVFP4 element rule over every row of a table (the
+  dense dequant a tied lm_head needs; same page, "Comments" and "Risks").
 * ``nv_embedding_gather`` / ``nv_embedding_gather_at`` -- NVFP4 gather-dequant,
   "sgl-project/sglang pull 34222" (prhub digest), "Implementation breakdown"
   item 2 and the ``reference_dequant`` test oracle: value * (e4m3 block scale *
@@ -101,6 +103,9 @@ def bind(path: str):
         _P64, _P8, _P8, ctypes.c_float, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         _P64, _P64, ctypes.c_int64, _P16]
     lib.oracle_nv_embedding_gather_at.restype = None
+    lib.oracle_nv_dequant.argtypes = [_P8, _P8, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_int64, _P16, ctypes.c_int]
+    lib.oracle_nv_dequant.restype = None
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -208,6 +213,20 @@ class Oracle:
             float(np.float32(global_scale)), vocab, hidden, group_size,
             _ptr(rows, ctypes.c_int64), _ptr(cols, ctypes.c_int64), rows.size,
             _ptr(out, ctypes.c_uint16))
+        return out
+
+    def nv_dequant(self, weight, scales, global_scale, group_size: int = 16,
+                   threads: int = 1) -> np.ndarray:
+        """Whole-table dequant: uint16[vocab, hidden]."""
+        weight, scales = _u8(weight), _u8(scales)
+        rows, half = weight.shape
+        hidden = 2 * half
+        if scales.shape != (rows, hidden // group_size):
+            raise ValueError("scales must be [rows, hidden / group_size]")
+        out = np.empty((rows, hidden), dtype=np.uint16)
+        self.lib.oracle_nv_dequant(_ptr(weight, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                   float(np.float32(global_scale)), rows, hidden, group_size,
+                                   _ptr(out, ctypes.c_uint16), int(threads))
         return out
 
     def max_threads(self) -> int:

@@ -241,6 +241,25 @@ void oracle_nv_embedding_gather_at(const int64_t *ids, const uint8_t *weight,
     }
 }
 
+/* Dense dequant of a whole NVFP4 table: out[r, :] = decode(weight[r], scale[r])
+ * for r = 0..rows-1 -- the same element rule as the gather, for every row in
+ * order ("sgl-project/sglang pull 34222", "Comments" and "Risks": a tied lm_head
+ * needs the table itself, which the gather-only method cannot serve). */
+void oracle_nv_dequant(const uint8_t *weight, const uint8_t *scales, float global_scale,
+                       int64_t rows, int64_t hidden, int64_t group_size, uint16_t *out,
+                       int threads) {
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1)
+#endif
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint8_t *weight_row = weight + r * (hidden / 2);
+        const uint8_t *scale_row = scales + r * (hidden / group_size);
+        for (int64_t c = 0; c < hidden; ++c)
+            out[r * hidden + c] = nv_element(weight_row, scale_row, global_scale, c, group_size);
+    }
+}
+
 /* Threads OpenMP would use (1 when built without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -384,6 +384,17 @@ def pin_nv_gather_invariants(o):
     assert np.array_equal(got[0], dense[5]) and np.array_equal(got[3], dense[7])
 
 
+def pin_nv_dense_is_gather_of_every_row(o):
+    """The dense dequant of a table equals the gather of ids 0..vocab-1, row by row,
+    and its row r does not depend on the other rows."""
+    x = inputs.nv_random(23, 2880, (1,), seed=51)
+    dense = o.nv_dequant(x.weight, x.scales, x.global_scale)
+    gathered, bad = o.nv_embedding_gather(np.arange(23), x.weight, x.scales, x.global_scale)
+    assert bad == 0 and np.array_equal(dense, gathered)
+    one = o.nv_dequant(x.weight[7:8], x.scales[7:8], x.global_scale)
+    assert np.array_equal(one[0], dense[7])
+
+
 def pin_nv_sampled_equals_full(o):
     x = inputs.nv_random(30, 64, (9,), seed=41)
     full, _ = o.nv_embedding_gather(x.ids, x.weight, x.scales, x.global_scale)

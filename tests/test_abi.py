@@ -55,7 +55,7 @@ def test_status_strings(lib):
     for code in range(1, 9):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 100
+    assert lib.fp4_abi_version() == 101
 
 
 def test_mx_host_validation(lib):
@@ -84,6 +84,17 @@ def test_nv_host_validation(lib):
     assert f(*args(0, 10, 64, 16)) == fp4.Status.OK               # no ids: no launch
     assert f(*args(4, 0, 64, 16)) == fp4.Status.ERR_SHAPE         # ids but empty table
     assert f(*args(4, 10, 64, 16)) == fp4.Status.ERR_NULL_PTR
+
+
+def test_nv_dequant_host_validation(lib):
+    f = lib.fp4_nv_dequant
+    args = lambda r, h, g: (None, None, None, r, h, g, None, None)
+    assert f(*args(4, 100, 16)) == fp4.Status.ERR_GROUP
+    assert f(*args(4, 96, 32)) == fp4.Status.ERR_UNSUPPORTED
+    assert f(*args(-1, 64, 16)) == fp4.Status.ERR_SHAPE
+    assert f(*args(4, 0, 16)) == fp4.Status.ERR_SHAPE
+    assert f(*args(0, 64, 16)) == fp4.Status.OK
+    assert f(*args(4, 64, 16)) == fp4.Status.ERR_NULL_PTR
 
 
 def test_binding_refuses_cpu_tensors():

@@ -328,3 +328,76 @@ def test_side_stream_and_graph_capture(ref):
     torch.cuda.synchronize()
     assert_same(bits(out_m), want_m, "graph mx")
     assert_same(bits(out_n), want_n, "graph nv")
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 dense dequant of a whole table
+# ---------------------------------------------------------------------------
+
+def gpu_dense(x, out=None):
+    return fp4.fp4_nv_dequant(torch.from_numpy(x.weight).to(DEV), torch.from_numpy(x.scales).to(DEV),
+                              torch.tensor([x.global_scale], dtype=torch.float32, device=DEV),
+                              out=out)
+
+
+@pytest.mark.parametrize("rows,hidden,seed", [(1, 16, 1), (5, 48, 2), (64, 2880, 3),
+                                              (300, 8192, 4), (7, 4096 + 16, 5)])
+def test_nv_dequant_shapes(ref, rows, hidden, seed):
+    """Flat kernel (hidden < 256) and row-segment kernel with ragged segments."""
+    x = inputs.nv_random(rows, hidden, (1,), seed)
+    assert_same(bits(gpu_dense(x)), ref.nv_dequant(x.weight, x.scales, x.global_scale),
+                f"dense {rows}x{hidden}")
+
+
+def test_nv_dequant_table_32k(ref):
+    x = inputs.nv_embedding_32k()
+    assert_same(bits(gpu_dense(x)), ref.nv_dequant(x.weight, x.scales, x.global_scale, threads=THREADS),
+                "dense 32000x4096")
+
+
+def test_nv_dequant_table_200k_full(ref):
+    x = inputs.nv_embedding_200k()
+    out = gpu_dense(x)
+    got = bits(out)
+    del out
+    torch.cuda.empty_cache()
+    assert_same(got, ref.nv_dequant(x.weight, x.scales, x.global_scale, threads=THREADS),
+                "dense 200000x8192")
+
+
+def test_nv_dequant_matches_gather_of_every_id():
+    x = inputs.nv_random(97, 2880, (1,), seed=6)
+    dense = bits(gpu_dense(x))
+    gathered = bits(gpu_nv(x, ids=np.arange(97)))
+    assert np.array_equal(dense, gathered)
+
+
+@pytest.mark.parametrize("w_off,o_off", [(1, 0), (0, 2)])
+def test_nv_dequant_unaligned(ref, w_off, o_off):
+    x = inputs.nv_random(19, 160, (1,), seed=7 + w_off)
+    lib = fp4.load()
+    wbuf = torch.zeros(x.weight.size + 16, dtype=torch.uint8, device=DEV)
+    wbuf[w_off:w_off + x.weight.size] = torch.from_numpy(x.weight.reshape(-1)).to(DEV)
+    obuf = torch.zeros(19 * 160 * 2 + 32, dtype=torch.uint8, device=DEV)
+    s = torch.from_numpy(x.scales).to(DEV)
+    gs = torch.tensor([x.global_scale], dtype=torch.float32, device=DEV)
+    code = lib.fp4_nv_dequant(wbuf.data_ptr() + w_off, s.data_ptr(), gs.data_ptr(), 19, 160, 16,
+                              obuf.data_ptr() + o_off, torch.cuda.current_stream().cuda_stream)
+    assert code == 0
+    got = obuf[o_off:o_off + 19 * 160 * 2].cpu().numpy().view(np.uint16)
+    assert_same(got, ref.nv_dequant(x.weight, x.scales, x.global_scale), "dense unaligned")
+
+
+def test_nv_dequant_canaries_and_guards(ref):
+    x = inputs.nv_random(13, 2880, (1,), seed=8)
+    n = x.vocab * x.hidden
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 0x5A5A, dtype=torch.int16, device=DEV)
+    gpu_dense(x, out=buf[guard:guard + n].view(torch.bfloat16).view(13, 2880))
+    host = buf.cpu().numpy().view(np.uint16)
+    assert np.all(host[:guard] == 0x5A5A) and np.all(host[guard + n:] == 0x5A5A)
+    assert_same(host[guard:guard + n], ref.nv_dequant(x.weight, x.scales, x.global_scale), "dense canary")
+    with pytest.raises(fp4.Fp4Error) as e:
+        fp4.fp4_nv_dequant(torch.zeros(4, 50, dtype=torch.uint8, device=DEV),
+                           torch.zeros(4, 6, dtype=torch.uint8, device=DEV), torch.ones(1, device=DEV))
+    assert e.value.code == fp4.Status.ERR_GROUP

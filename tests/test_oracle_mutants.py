@@ -52,6 +52,11 @@ MUTATIONS = [
     ("const uint8_t *scale_row = scales + id * (hidden / group_size);",
      "const uint8_t *scale_row = scales + t * (hidden / group_size);",
      "scale row gathered by position not id"),
+    ("const uint8_t *scale_row = scales + r * (hidden / group_size);",
+     "const uint8_t *scale_row = scales + r * (hidden / 16 / group_size);",
+     "dense dequant scale row pitch wrong"),
+    ("out[r * hidden + c] = nv_element(", "out[r * (hidden / 2) + c] = nv_element(",
+     "dense dequant output row pitch wrong"),
     ("if (id < 0 || id >= vocab) {\n            for", "if (id < 0 || id > vocab) {\n            for",
      "last valid id off by one"),
 ]
