@@ -38,6 +38,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -46,7 +48,7 @@ METRIC = "decoded FP4 elements/sec and achieved HBM GB/s (% of GB300 peak), 1 GP
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("step", "mx_moe", "mx_stress", "mx_exhaustive", "nv_embedding_200k",
-             "nv_embedding_32k", "nv_dequant_200k", "nv_dequant_32k")
+             "nv_embedding_32k", "nv_dequant_200k", "nv_dequant_32k", "mx_quantize_moe")
 
 
 # ---------------------------------------------------------------------------
@@ -323,6 +325,46 @@ class NvDenseOp:
         return f"rows of the {self.x.name} table"
 
 
+class MxQuantOp:
+    """fp4_mx_quantize of one bf16 [rows, k] tensor."""
+    kind, kernel = "mx_quantize", "mx_quantize_words_kernel"
+
+    def __init__(self, w):
+        self.w = w
+        self.elems = w.n_elems
+        self.bytes = w.algorithmic_bytes()
+        self.min_bytes = self.bytes
+        self.units, self.elems_per_unit = w.rows, w.k
+
+    def to_device(self, torch, dev):
+        self.x = torch.from_numpy(self.w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.p = torch.empty(self.w.rows, self.w.k // 2, dtype=torch.uint8, device=dev)
+        self.s = torch.empty(self.w.rows, self.w.k // 32, dtype=torch.uint8, device=dev)
+
+    def launch(self, fp4, stream):
+        fp4.fp4_mx_quantize(self.x, self.p, self.s, stream=stream)
+
+    def e2e_jobs(self, torch, fp4, chunks):
+        hx = torch.from_numpy(self.w.x.view(np.int16)).pin_memory().view(torch.bfloat16)
+        hp = torch.empty(self.p.shape, dtype=torch.uint8).pin_memory()
+        hs = torch.empty(self.s.shape, dtype=torch.uint8).pin_memory()
+        jobs = []
+        for r0, r1 in _row_chunks(self.w.rows, chunks):
+            def fn(st, r0=r0, r1=r1):
+                self.x[r0:r1].copy_(hx[r0:r1], non_blocking=True)
+                fp4.fp4_mx_quantize(self.x[r0:r1], self.p[r0:r1], self.s[r0:r1], stream=st)
+                hp[r0:r1].copy_(self.p[r0:r1], non_blocking=True)
+                hs[r0:r1].copy_(self.s[r0:r1], non_blocking=True)
+            jobs.append((hx[r0:r1].numel() * 2, hp[r0:r1].numel() + hs[r0:r1].numel(), fn))
+        return jobs
+
+    def oracle_units(self, o, n, threads):
+        o.mx_quantize(self.w.x[:n], threads)
+
+    def sample_name(self):
+        return f"rows of {self.w.name}"
+
+
 def load_workload(name: str):
     """The ops of one step of the named workload, in launch order."""
     from block_scaled_fp4_mx_gb300 import inputs
@@ -336,6 +378,7 @@ def load_workload(name: str):
         "nv_embedding_32k": lambda: [NvGatherOp(inputs.nv_embedding_32k())],
         "nv_dequant_200k": lambda: [NvDenseOp(inputs.nv_embedding_200k())],
         "nv_dequant_32k": lambda: [NvDenseOp(inputs.nv_embedding_32k())],
+        "mx_quantize_moe": lambda: [MxQuantOp(w) for w in inputs.bf16_moe()],
     }
     return table[name]()
 

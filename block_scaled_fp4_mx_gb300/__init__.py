@@ -12,6 +12,9 @@ status raise.
   applied as a wrapping int16 add of (E-127)<<7 into the bf16 exponent field,
   zero codes forced to +0.0 ("vllm-project/vllm pull 51583", "Motivation",
   "Implementation breakdown").
+* ``fp4_mx_quantize(x_bf16)`` -- the inverse direction: bf16 -> (packed E2M1
+  codes, E8M0 scales), by the OCP MX v1.0 conversion (the pages name the step,
+  MXFP4QuantizeUtil.quantize, but not its rule).
 * ``fp4_nv_embedding_gather(ids, weight, block_scale, global_scale)`` -- NVFP4
   embedding lookup dequantised at gather time: value * (e4m3 block scale * fp32
   global scale) in fp32, rounded to bf16 ("sgl-project/sglang pull 34222",
@@ -23,7 +26,8 @@ from __future__ import annotations
 
 from ._lib import Status, last_error, library_path, load, status_string  # noqa: F401
 
-__all__ = ["fp4_mx_unpack", "fp4_nv_embedding_gather", "fp4_nv_dequant", "fp4_status_string",
+__all__ = ["fp4_mx_unpack", "fp4_mx_quantize", "fp4_nv_embedding_gather", "fp4_nv_dequant",
+           "fp4_status_string",
            "Fp4Error",
            "Status", "load", "library_path"]
 
@@ -177,3 +181,29 @@ def fp4_nv_dequant(weight, block_scale, global_scale, group_size: int = 16, out=
     if code != Status.OK:
         raise Fp4Error("fp4_nv_dequant", code)
     return out
+
+
+def fp4_mx_quantize(x, packed_out=None, scales_out=None, stream=None):
+    """bf16 [..., k] (k % 32 == 0) -> (packed uint8 [..., k/2], E8M0 uint8 [..., k/32]):
+    shared exponent floor(log2 amax) - 2 per 32 values, elements rounded to nearest
+    even on the E2M1 grid with saturation at 6 (OCP MX v1.0)."""
+    torch = _torch()
+    _check_cuda(x, "x", (torch.bfloat16, torch.int16, torch.uint16))
+    if x.dim() < 1 or x.shape[-1] % 32:
+        raise ValueError("x must have a last dimension that is a multiple of 32")
+    k = x.shape[-1]
+    rows = x.numel() // k if k else 0
+    p_shape, s_shape = (*x.shape[:-1], k // 2), (*x.shape[:-1], k // 32)
+    if packed_out is None:
+        packed_out = torch.empty(p_shape, dtype=torch.uint8, device=x.device)
+    if scales_out is None:
+        scales_out = torch.empty(s_shape, dtype=torch.uint8, device=x.device)
+    _check_cuda(packed_out, "packed_out", (torch.uint8,))
+    _check_cuda(scales_out, "scales_out", (torch.uint8,))
+    if tuple(packed_out.shape) != p_shape or tuple(scales_out.shape) != s_shape:
+        raise ValueError(f"outputs must have shapes {p_shape} and {s_shape}")
+    code = load().fp4_mx_quantize(_ptr(x), _ptr(packed_out), _ptr(scales_out), rows, k,
+                                  _stream_handle(stream, x.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_mx_quantize", code)
+    return packed_out, scales_out

@@ -27,6 +27,7 @@ class Status(enum.IntEnum):
     ERR_CUDA = 6
     ERR_POINTER = 7
     ERR_ALIAS = 8
+    ERR_ALIGN = 9
 
 
 # Every function the header declares, with its ctypes signature.
@@ -37,6 +38,7 @@ SIGNATURES = {
     "fp4_nv_embedding_gather": ([_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp],
                                 ctypes.c_int),
     "fp4_nv_dequant": ([_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp], ctypes.c_int),
+    "fp4_mx_quantize": ([_vp, _vp, _vp, _i64, _i64, _vp], ctypes.c_int),
     "fp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "fp4_last_error": ([], ctypes.c_char_p),
     "fp4_abi_version": ([], ctypes.c_int),

@@ -59,6 +59,10 @@ fp4_status check_device_pointer(const void *p, int device) {
     return FP4_ERR_POINTER;
 }
 
+bool misaligned(const void *p, uintptr_t alignment) {
+    return p != nullptr && reinterpret_cast<uintptr_t>(p) % alignment != 0;
+}
+
 fp4_status check_pointers(const void *const *ptrs, int n) {
     int device = 0;
     const cudaError_t err = cudaGetDevice(&device);
@@ -109,6 +113,7 @@ FP4_EXPORT fp4_status fp4_mx_unpack(const uint8_t *packed, const uint8_t *scales
     if (rows > INT64_MAX / 2 / k) return FP4_ERR_SHAPE;  // rows * k * 2 bytes must fit
     if (packed == nullptr || scales_e8m0 == nullptr || out_bf16 == nullptr)
         return FP4_ERR_NULL_PTR;
+    if (misaligned(out_bf16, 2)) return FP4_ERR_ALIGN;
     const int64_t n = rows * k;
     const uint64_t out_bytes = (uint64_t)n * 2;
     if (overlaps(out_bf16, out_bytes, packed, (uint64_t)n / 2) ||
@@ -139,6 +144,9 @@ FP4_EXPORT fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_id
     if (ids == nullptr || weight == nullptr || block_scale_e4m3 == nullptr ||
         global_scale == nullptr || out_bf16 == nullptr)
         return FP4_ERR_NULL_PTR;
+    if (misaligned(ids, 8) || misaligned(global_scale, 4) || misaligned(out_bf16, 2) ||
+        misaligned(err_flag, 4))
+        return FP4_ERR_ALIGN;
     const uint64_t out_bytes = (uint64_t)num_ids * (uint64_t)hidden * 2;
     const uint64_t w_bytes = (uint64_t)vocab * (uint64_t)hidden / 2;
     const uint64_t s_bytes = (uint64_t)vocab * (uint64_t)hidden / 16;
@@ -161,6 +169,30 @@ FP4_EXPORT fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_id
     return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_nv_embedding_gather launch");
 }
 
+FP4_EXPORT fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_out,
+                                      uint8_t *scales_e8m0_out, int64_t rows, int64_t k,
+                                      fp4_stream_t stream) {
+    clear_error();
+    if (rows < 0 || k < 0 || k % 32 != 0) return FP4_ERR_SHAPE;
+    if (rows == 0 || k == 0) return FP4_OK;
+    if (rows > INT64_MAX / 2 / k) return FP4_ERR_SHAPE;
+    if (in_bf16 == nullptr || packed_out == nullptr || scales_e8m0_out == nullptr)
+        return FP4_ERR_NULL_PTR;
+    if (misaligned(in_bf16, 2)) return FP4_ERR_ALIGN;
+    const int64_t n = rows * k;
+    const uint64_t in_bytes = (uint64_t)n * 2;
+    if (overlaps(packed_out, (uint64_t)n / 2, in_bf16, in_bytes) ||
+        overlaps(scales_e8m0_out, (uint64_t)n / 32, in_bf16, in_bytes) ||
+        overlaps(packed_out, (uint64_t)n / 2, scales_e8m0_out, (uint64_t)n / 32))
+        return FP4_ERR_ALIAS;
+    const void *ptrs[] = {in_bf16, packed_out, scales_e8m0_out};
+    const fp4_status s = check_pointers(ptrs, 3);
+    if (s != FP4_OK) return s;
+    const cudaError_t err = fp4mx::launch_mx_quantize(in_bf16, packed_out, scales_e8m0_out, n,
+                                                      (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_quantize launch");
+}
+
 FP4_EXPORT fp4_status fp4_nv_dequant(const uint8_t *weight, const uint8_t *block_scale_e4m3,
                                      const float *global_scale, int64_t rows, int64_t hidden,
                                      int64_t group_size, uint16_t *out_bf16,
@@ -174,6 +206,7 @@ FP4_EXPORT fp4_status fp4_nv_dequant(const uint8_t *weight, const uint8_t *block
     if (weight == nullptr || block_scale_e4m3 == nullptr || global_scale == nullptr ||
         out_bf16 == nullptr)
         return FP4_ERR_NULL_PTR;
+    if (misaligned(global_scale, 4) || misaligned(out_bf16, 2)) return FP4_ERR_ALIGN;
     const uint64_t out_bytes = (uint64_t)rows * (uint64_t)hidden * 2;
     if (overlaps(out_bf16, out_bytes, weight, (uint64_t)rows * (uint64_t)hidden / 2) ||
         overlaps(out_bf16, out_bytes, block_scale_e4m3, (uint64_t)rows * (uint64_t)hidden / 16) ||
@@ -198,10 +231,11 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
     case FP4_ERR_CUDA: return "CUDA runtime error";
     case FP4_ERR_POINTER: return "pointer is not device-accessible CUDA memory";
     case FP4_ERR_ALIAS: return "output overlaps an input";
+    case FP4_ERR_ALIGN: return "pointer not aligned to its element type";
     }
     return "unknown status";
 }
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 101; }
+FP4_EXPORT int fp4_abi_version(void) { return 102; }

@@ -24,6 +24,10 @@ cudaError_t launch_nv_dequant(const uint8_t *weight, const uint8_t *scales,
                               const float *global_scale, int64_t rows, int64_t hidden,
                               uint16_t *out, cudaStream_t stream);
 
+// Quantise n_elems (a positive multiple of 32) bf16 values to MXFP4.
+cudaError_t launch_mx_quantize(const uint16_t *in, uint8_t *packed, uint8_t *scales,
+                               int64_t n_elems, cudaStream_t stream);
+
 // Resident CTAs per SM x SM count for `kernel` at `threads` threads, cached per
 // device; a grid no larger than this runs in one wave.
 int max_resident_ctas(const void *kernel, int threads, int slot);

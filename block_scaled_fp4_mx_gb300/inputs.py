@@ -27,6 +27,8 @@ nv_embedding_200k   vocab 200,000 x hidden 8,192; scales as above; 16,384 ids
 mx_stress           2^30 packed bytes; each nibble a zero code with p = 0.3
                     (0x0 or 0x8, half each), else uniform over the 14 nonzero
                     codes; E per block uniform over {0, 107, 127, 137, 255}
+bf16_moe            (input of the quantiser) gate+up and down MoE weights as bf16,
+                    standard normal / 10 as the pages' MoE test draws them
 ==================  ==========================================================
 """
 from __future__ import annotations
@@ -171,6 +173,63 @@ def zipf_ids(rng: np.random.Generator, n: int, vocab: int, s: float) -> np.ndarr
     cdf /= cdf[-1]
     u = rng.random(n)
     return np.minimum(np.searchsorted(cdf, u, side="right"), vocab - 1).astype(np.int64)
+
+
+def bf16_normal_bits(rng: np.random.Generator, n: int, scale: float = 0.1) -> np.ndarray:
+    """bf16 bit patterns of standard-normal draws times ``scale`` (torch's
+    round-to-nearest-even float32 -> bfloat16 cast)."""
+    import torch
+
+    out = np.empty(n, dtype=np.uint16)
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        v = rng.standard_normal(e - s, dtype=np.float32) * np.float32(scale)
+        out[s:e] = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return out
+
+
+@dataclass
+class Bf16Input:
+    x: np.ndarray  # uint16 bf16 bit patterns [rows, k]
+    name: str = ""
+
+    @property
+    def rows(self) -> int:
+        return self.x.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.x.shape[1]
+
+    @property
+    def n_elems(self) -> int:
+        return self.x.size
+
+    def algorithmic_bytes(self) -> int:
+        """Quantise: read bf16, write packed codes + scales."""
+        return 2 * self.n_elems + self.n_elems // 2 + self.n_elems // MX_BLOCK
+
+
+def bf16_moe(seed: int = 5) -> list[Bf16Input]:
+    """MoE expert weights in bf16 (gate+up 32 x 5760 rows, down 32 x 2880 rows, 2880
+    columns), standard normal / 10: the input the pages' MoE test quantises."""
+    rng = np.random.default_rng(seed)
+    return [Bf16Input(bf16_normal_bits(rng, rows * 2880).reshape(rows, 2880), name=f"bf16_moe_{nm}")
+            for nm, rows in (("gate_up", 32 * 5760), ("down", 32 * 2880))]
+
+
+def bf16_blocks_wide_range(n_blocks: int, seed: int) -> np.ndarray:
+    """uint16 [n_blocks, 32] bf16 blocks spanning the exponent range: normal draws
+    times 2^k with k per block in [-140, 120] (so zeros, subnormals and values near
+    the top of the range occur), a third of the entries of every 7th block zero,
+    every 11th block negated."""
+    import torch
+
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((n_blocks, 32)) * np.exp2(rng.integers(-140, 121, (n_blocks, 1)))
+    x[::7, ::3] = 0.0
+    x[::11] *= -1
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
 # ---------------------------------------------------------------------------

@@ -2,7 +2,7 @@
  * fp4mx.h -- C ABI of a GB300 (sm_103a) library that decodes block-scaled FP4
  * (E2M1) data into bf16.
  *
- * Three operations, each one CUDA kernel launch on the caller's stream:
+ * Four operations, each one CUDA kernel launch on the caller's stream:
  *
  *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
  *                             a wrapping 16-bit integer add into the bf16 exponent
@@ -12,6 +12,7 @@
  *                             value is multiplied by (block scale * global scale)
  *                             in fp32 and rounded to bf16 (nearest, ties to even).
  *   fp4_nv_dequant            the same NVFP4 decode over every row of a table.
+ *   fp4_mx_quantize           bf16 to MXFP4 (the inverse direction of the unpack).
  *
  * Conventions shared by every entry point:
  *   - Pointers named "device" must be device-accessible CUDA allocations
@@ -28,9 +29,10 @@
  *     nothing is launched and the outputs are untouched. A call with zero
  *     elements returns FP4_OK without launching.
  *   - Outputs must not overlap inputs (FP4_ERR_ALIAS).
- *   - Any alignment is accepted; 16-byte aligned outputs with 4-byte aligned
- *     packed inputs take the vectorised kernels, others a scalar kernel with the
- *     same results.
+ *   - Byte buffers may have any alignment; bf16 (uint16_t), int32, int64 and
+ *     float buffers must be aligned to their element size (else FP4_ERR_ALIGN).
+ *     16-byte aligned bf16 buffers with 4-byte aligned packed buffers take the
+ *     vectorised kernels, others a scalar kernel with the same results.
  *   - Calls are thread-safe and may be captured into CUDA graphs (no host
  *     synchronisation, no allocation, no host-to-device copy).
  */
@@ -55,7 +57,8 @@ typedef enum fp4_status {
     FP4_ERR_INDEX = 5,       /* value written to err_flag when an id is out of range */
     FP4_ERR_CUDA = 6,        /* the CUDA runtime reported an error (see fp4_last_error) */
     FP4_ERR_POINTER = 7,     /* a pointer is not device-accessible memory           */
-    FP4_ERR_ALIAS = 8        /* an output range overlaps an input range             */
+    FP4_ERR_ALIAS = 8,       /* an output range overlaps an input range             */
+    FP4_ERR_ALIGN = 9        /* a uint16/int32/int64/float pointer not aligned to its type */
 } fp4_status;
 
 /*
@@ -120,6 +123,32 @@ fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_ids, const ui
                                    uint16_t *out_bf16, int32_t *err_flag, fp4_stream_t stream);
 
 /*
+ * fp4_mx_quantize -- bf16 to MXFP4: E2M1 codes plus one E8M0 scale per 32.
+ *
+ * The inverse direction of fp4_mx_unpack. "vllm-project/vllm pull 51583"
+ * (prhub digest), "Key source snippets": the test quantises bf16 weights with
+ * MXFP4QuantizeUtil.quantize into packed codes and per-32 scales, the format
+ * fp4_mx_unpack reads; the pages do not print the rule. The rule used is the
+ * OCP Microscaling (MX) v1.0 conversion, per block of 32 consecutive values:
+ *     s    = floor(log2(max |x_i|)) - 2, clamped below at -127  (E8M0 = s + 127;
+ *            an all-zero block gets E8M0 = 0)
+ *     code = x_i / 2^s rounded to the nearest of {0, 0.5, 1, 1.5, 2, 3, 4, 6}, a tie
+ *            to the even code, magnitudes above 6 saturated to 6; the sign bit of
+ *            x_i is kept (so -0.0 and negatives that round to zero give code 8)
+ *     a block holding Inf or NaN gets E8M0 = 0xFF (the MX NaN scale), codes 0.
+ * For every block with E8M0 in [2, 252], fp4_mx_unpack(fp4_mx_quantize(x))
+ * returns the nearest MXFP4 values; on values it produced itself it is exact.
+ *
+ *   in_bf16          device, uint16[rows * k] bf16 bits, row-major [rows, k], 2-byte aligned
+ *   packed_out       device, uint8[rows * k / 2] (even element in the low nibble)
+ *   scales_e8m0_out  device, uint8[rows * k / 32]
+ *   rows, k          rows >= 0, k >= 0, k % 32 == 0 (else FP4_ERR_SHAPE)
+ *   stream           CUDA stream the kernel is enqueued on
+ */
+fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_out, uint8_t *scales_e8m0_out,
+                           int64_t rows, int64_t k, fp4_stream_t stream);
+
+/*
  * fp4_nv_dequant -- dequantise a whole NVFP4 table (every row, in order).
  *
  * The dense counterpart of fp4_nv_embedding_gather: out[r][c] is what the
@@ -149,7 +178,8 @@ const char *fp4_status_string(fp4_status status);
  * until this thread's next call into the library. */
 const char *fp4_last_error(void);
 
-/* Version of this ABI (major * 100 + minor): 101 adds fp4_nv_dequant. */
+/* Version of this ABI (major * 100 + minor): 101 adds fp4_nv_dequant, 102 adds
+ * fp4_mx_quantize and FP4_ERR_ALIGN. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

@@ -12,6 +12,10 @@ Functions and the passages they follow (web pages cited by title and section):
   "vllm-project/vllm pull 51583" (prhub digest), "Motivation" and
   "Implementation breakdown" items 1-2: E2M1 code -> bf16 bits, E8M0 scale as a
   wrapping int16 add of (E-127)<<7, zero codes forced to +0.0 lane by lane.
+* ``mx_quantize`` -- the step before the unpack (bf16 -> E2M1 codes + E8M0 per
+  32), named but not printed by the same page; written from the OCP MX v1.0
+  conversion (shared exponent floor(log2 amax) - 2, nearest-even rounding onto
+  the E2M1 grid, saturation at 6).
 * ``e4m3_to_f32``, ``f32_to_bf16_rne``, ``e2m1_bf16_bits`` -- the element
   conversions those steps use (OCP FP8 E4M3 definition; IEEE round to nearest
   even into bf16; the E2M1 codebook).
@@ -106,6 +110,8 @@ def bind(path: str):
     lib.oracle_nv_dequant.argtypes = [_P8, _P8, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_int64, _P16, ctypes.c_int]
     lib.oracle_nv_dequant.restype = None
+    lib.oracle_mx_quantize.argtypes = [_P16, ctypes.c_int64, _P8, _P8, ctypes.c_int]
+    lib.oracle_mx_quantize.restype = None
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -178,6 +184,24 @@ class Oracle:
                                      _ptr(idx, ctypes.c_int64), idx.size,
                                      _ptr(out, ctypes.c_uint16))
         return out
+
+    def mx_quantize(self, x_bf16_bits, threads: int = 1):
+        """bf16 bit patterns (uint16[..., k], k % 32 == 0) -> (packed uint8[..., k/2],
+        E8M0 scales uint8[..., k/32])."""
+        x = np.ascontiguousarray(x_bf16_bits)
+        if x.dtype != np.uint16:
+            raise TypeError("expected uint16 bf16 bit patterns")
+        shape = x.shape
+        if shape[-1] % 32:
+            raise ValueError("last dimension must be a multiple of 32")
+        flat = x.reshape(-1)
+        packed = np.empty(flat.size // 2, dtype=np.uint8)
+        scales = np.empty(flat.size // 32, dtype=np.uint8)
+        self.lib.oracle_mx_quantize(_ptr(flat, ctypes.c_uint16), flat.size,
+                                    _ptr(packed, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                    int(threads))
+        return (packed.reshape(*shape[:-1], shape[-1] // 2),
+                scales.reshape(*shape[:-1], shape[-1] // 32))
 
     # -- NVFP4 ----------------------------------------------------------------
     def nv_embedding_gather(self, ids, weight, scales, global_scale, group_size: int = 16,

@@ -260,6 +260,92 @@ void oracle_nv_dequant(const uint8_t *weight, const uint8_t *scales, float globa
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* MXFP4 quantise: bf16 -> E2M1 codes + one E8M0 scale per 32 elements       */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name the step that produces MXFP4 weights
+ * ("vllm-project/vllm pull 51583", "Key source snippets": MXFP4QuantizeUtil
+ * .quantize returns packed codes and per-32 scales) but do not print its rule.
+ * Reading: the OCP Microscaling (MX) v1.0 conversion.
+ *   - shared exponent s = floor(log2(max_i |x_i|)) - 2 (2 = the exponent of
+ *     E2M1's largest value 6 = 1.5 * 2^2), clamped below at -127; the E8M0 byte
+ *     is s + 127. An all-zero block takes the smallest scale, E8M0 = 0.
+ *   - each element is x_i / 2^s rounded to the nearest E2M1 magnitude
+ *     {0, 0.5, 1, 1.5, 2, 3, 4, 6}; on a tie the magnitude with an even code
+ *     (mantissa bit 0) wins; magnitudes above 6 saturate to 6. The sign bit of
+ *     x_i is kept (so -0.0 and small negatives that round to zero give code 8).
+ *   - a block holding Inf or NaN gets the E8M0 NaN byte 0xFF and zero codes. */
+static double bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static unsigned nearest_e2m1_magnitude(double a) {
+    unsigned best = 0;
+    double best_err = fabs(a - (double)kMagnitude[0]);
+    for (unsigned m = 1; m < 8; ++m) {
+        double err = fabs(a - (double)kMagnitude[m]);
+        if (err < best_err || (err == best_err && (m % 2) == 0 && (best % 2) == 1)) {
+            best = m;
+            best_err = err;
+        }
+    }
+    return best; /* a > 6 is nearest to 6: saturation */
+}
+
+static void mx_quantize_block(const uint16_t *x, uint8_t *packed16, uint8_t *scale) {
+    double amax = 0.0;
+    int finite = 1;
+    for (int i = 0; i < 32; ++i) {
+        double v = bf16_value(x[i]);
+        if (isnan(v) || isinf(v))
+            finite = 0;
+        else if (fabs(v) > amax)
+            amax = fabs(v);
+    }
+    if (!finite) {
+        *scale = 0xFF;
+        memset(packed16, 0, 16);
+        return;
+    }
+    int shared = -127;
+    if (amax > 0.0) {
+        int e;
+        frexp(amax, &e); /* amax = f * 2^e with f in [0.5, 1): floor(log2 amax) = e - 1 */
+        shared = (e - 1) - 2;
+        if (shared < -127)
+            shared = -127;
+    }
+    *scale = (uint8_t)(shared + 127);
+    for (int i = 0; i < 32; i += 2) {
+        unsigned codes[2];
+        for (int h = 0; h < 2; ++h) {
+            double v = bf16_value(x[i + h]);
+            double scaled = ldexp(fabs(v), -shared); /* exact: a power-of-two scaling */
+            unsigned code = nearest_e2m1_magnitude(scaled);
+            if (signbit(v))
+                code |= 8u;
+            codes[h] = code;
+        }
+        packed16[i / 2] = (uint8_t)(codes[0] | (codes[1] << 4));
+    }
+}
+
+/* Quantise n_elems (a multiple of 32) bf16 values: packed[n/2], scales[n/32]. */
+void oracle_mx_quantize(const uint16_t *in_bf16, int64_t n_elems, uint8_t *packed,
+                        uint8_t *scales, int threads) {
+    int64_t n_blocks = n_elems / 32;
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1)
+#endif
+    for (int64_t b = 0; b < n_blocks; ++b)
+        mx_quantize_block(in_bf16 + b * 32, packed + b * 16, scales + b);
+}
+
 /* Threads OpenMP would use (1 when built without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -281,6 +281,101 @@ def pin_mx_sampled_equals_full(o):
 
 
 # ---------------------------------------------------------------------------
+# pins: MXFP4 quantise (bf16 -> codes + E8M0)
+# ---------------------------------------------------------------------------
+
+def _bf16_bits(values) -> np.ndarray:
+    """bf16 bit patterns of float64 values (rounded by torch)."""
+    t = torch.as_tensor(np.asarray(values, dtype=np.float64)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().astype(np.uint16)
+
+
+def _quantize_test_blocks(seed=61, n_blocks=4000):
+    return inputs.bf16_blocks_wide_range(n_blocks, seed)
+
+
+def pin_mx_quantize_scale_closed_form(o):
+    """The E8M0 byte of a finite block is max(exponent field of its bf16 amax - 2, 0):
+    floor(log2 amax) - 2 biased by 127, read straight off the bit pattern (an
+    all-zero or subnormal block takes byte 0)."""
+    x = _quantize_test_blocks()
+    _, scales = o.mx_quantize(x)
+    amax_field = ((x & 0x7FFF).max(axis=1) >> 7).astype(np.int64)
+    assert np.array_equal(scales.reshape(-1), np.maximum(amax_field - 2, 0).astype(np.uint8))
+
+
+def pin_mx_quantize_roundtrip_of_decoded_blocks(o):
+    """Decoding then quantising then decoding returns the same bf16 values for every
+    block the unpack represents exactly (E in [2, 252]): quantise is a right inverse
+    of the unpack on its own outputs."""
+    x = inputs.mx_random(64, 1024, seed=62, e_lo=2, e_hi=252, zero_fraction=True)
+    decoded = o.mx_unpack(x.packed, x.scales).reshape(64, 1024)
+    p2, s2 = o.mx_quantize(decoded)
+    assert np.array_equal(o.mx_unpack(p2, s2).reshape(64, 1024), decoded)
+
+
+def pin_mx_quantize_ties_and_saturation(o):
+    """Hand-worked rounding cases (nearest, ties to the even code, saturation at 6)."""
+    g = golden("mx_quantize_ties.txt")
+    for key in ("cases", "saturate"):
+        for pair in g[key]:
+            val, code = pair.split("=")
+            blk = np.zeros(32)
+            blk[0] = 6.0 if key == "cases" else 0.0
+            blk[1] = float(val)
+            p, s = o.mx_quantize(_bf16_bits(blk)[None, :])
+            assert s[0, 0] == 127, (val, s)
+            got = (p[0, 0] >> 4) & 0xF
+            assert got == int(code, 16), (val, hex(got), code)
+
+
+def pin_mx_quantize_specials(o):
+    """All-zero block: scale 0, codes 0 (-0.0 keeps its sign bit: code 8); a block
+    holding Inf or NaN: the E8M0 NaN byte 0xFF and zero codes."""
+    blk = np.zeros((4, 32))
+    blk[1, 5] = -0.0
+    blk[2, 9] = np.inf
+    blk[3, 0] = np.nan
+    bits = _bf16_bits(blk)
+    bits[1, 5] = 0x8000
+    p, s = o.mx_quantize(bits)
+    assert list(s.reshape(-1)) == [0, 0, 0xFF, 0xFF]
+    assert np.all(p[0] == 0) and np.all(p[2:] == 0)
+    assert (p[1, 2] >> 4) == 8 and np.count_nonzero(p[1]) == 1
+
+
+def pin_mx_quantize_sign_symmetry_and_order(o):
+    """quantise(-x) flips exactly the sign bit of every code; within one block the
+    decoded magnitude is non-decreasing in |x|."""
+    x = _quantize_test_blocks(seed=63, n_blocks=500)
+    p, s = o.mx_quantize(x)
+    pn, sn = o.mx_quantize(x ^ 0x8000)
+    assert np.array_equal(s, sn) and np.array_equal(pn, p ^ 0x88)
+    mags = np.abs(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy())
+    codes = nibble_codes(p).reshape(500, 32) & 7
+    order = np.argsort(mags, axis=1, kind="stable")
+    assert np.all(np.diff(np.take_along_axis(codes, order, axis=1).astype(int), axis=1) >= 0)
+
+
+def pin_mx_quantize_error_bound(o):
+    """Each decoded value is within half a grid step of the input (the grid step at
+    magnitude m is 0.5 below 2, 1 below 4, 2 above, times 2^s), except saturated
+    values, which decode to exactly +-6 * 2^s."""
+    x = _quantize_test_blocks(seed=64, n_blocks=2000)
+    x = x[(x & 0x7F80).max(axis=1) >> 7 >= 2]  # blocks whose scale is not clamped
+    p, s = o.mx_quantize(x)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    step = np.exp2(s.astype(np.float64) - 127)  # 2^s per block
+    mag = np.asarray([0, 0.5, 1, 1.5, 2, 3, 4, 6])[nibble_codes(p).reshape(x.shape) & 7]
+    deq = mag * step
+    a = np.abs(xv)
+    spacing = np.where(a < 2 * step, 0.5, np.where(a < 4 * step, 1.0, 2.0)) * step
+    sat = a > 6 * step
+    assert np.all(np.abs(a - deq)[~sat] <= spacing[~sat] / 2)
+    assert np.all(deq[sat] == (6 * step * np.ones_like(a))[sat])
+
+
+# ---------------------------------------------------------------------------
 # pins: NVFP4
 # ---------------------------------------------------------------------------
 

@@ -52,10 +52,10 @@ def test_only_api_symbols_exported():
 
 def test_status_strings(lib):
     assert fp4.fp4_status_string(0) == "ok"
-    for code in range(1, 9):
+    for code in range(1, 10):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 101
+    assert lib.fp4_abi_version() == 102
 
 
 def test_mx_host_validation(lib):
@@ -95,6 +95,36 @@ def test_nv_dequant_host_validation(lib):
     assert f(*args(4, 0, 16)) == fp4.Status.ERR_SHAPE
     assert f(*args(0, 64, 16)) == fp4.Status.OK
     assert f(*args(4, 64, 16)) == fp4.Status.ERR_NULL_PTR
+
+
+def test_mx_quantize_host_validation(lib):
+    f = lib.fp4_mx_quantize
+    assert f(None, None, None, 1, 33, None) == fp4.Status.ERR_SHAPE
+    assert f(None, None, None, -1, 32, None) == fp4.Status.ERR_SHAPE
+    assert f(None, None, None, 0, 64, None) == fp4.Status.OK
+    assert f(None, None, None, 2, 64, None) == fp4.Status.ERR_NULL_PTR
+    buf = ctypes.create_string_buffer(8192)
+    base = ctypes.addressof(buf)
+    base += (-base) % 16
+    assert f(base + 1, base + 4096, base + 6000, 1, 64, None) == fp4.Status.ERR_ALIGN
+    assert f(base, base + 64, base + 6000, 1, 64, None) == fp4.Status.ERR_ALIAS
+    assert f(base, base + 4096, base + 4100, 1, 256, None) == fp4.Status.ERR_ALIAS
+
+
+def test_alignment_refused_before_cuda(lib):
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = ctypes.addressof(buf)
+    base += (-base) % 16
+    # odd bf16 output of the unpack
+    assert lib.fp4_mx_unpack(base, base + 1024, base + 4097, 1, 64, None) == fp4.Status.ERR_ALIGN
+    # ids not 8-aligned, global scale not 4-aligned, output odd
+    g = lambda ids, gs, out: lib.fp4_nv_embedding_gather(ids, 2, base + 8192, base + 12288, gs, 4,
+                                                         64, 16, out, None, None)
+    assert g(base + 4, base + 16000, base + 20000) == fp4.Status.ERR_ALIGN
+    assert g(base, base + 16002, base + 20000) == fp4.Status.ERR_ALIGN
+    assert g(base, base + 16000, base + 20001) == fp4.Status.ERR_ALIGN
+    assert lib.fp4_nv_dequant(base + 8192, base + 12288, base + 16001, 4, 64, 16, base + 20000,
+                              None) == fp4.Status.ERR_ALIGN
 
 
 def test_binding_refuses_cpu_tensors():

@@ -401,3 +401,103 @@ def test_nv_dequant_canaries_and_guards(ref):
         fp4.fp4_nv_dequant(torch.zeros(4, 50, dtype=torch.uint8, device=DEV),
                            torch.zeros(4, 6, dtype=torch.uint8, device=DEV), torch.ones(1, device=DEV))
     assert e.value.code == fp4.Status.ERR_GROUP
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 quantise (bf16 -> codes + E8M0)
+# ---------------------------------------------------------------------------
+
+def gpu_quantize(x_bits: np.ndarray):
+    t = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).to(DEV).view(torch.bfloat16)
+    p, s = fp4.fp4_mx_quantize(t)
+    return p.cpu().numpy(), s.cpu().numpy()
+
+
+def assert_same_bytes(got, want, what):
+    got, want = got.reshape(-1), want.reshape(-1)
+    if not np.array_equal(got, want):
+        i = int(np.nonzero(got != want)[0][0])
+        raise AssertionError(f"{what}: first mismatch at {i}: gpu {got[i]:#04x} oracle {want[i]:#04x}")
+
+
+@pytest.mark.parametrize("n_blocks,seed", [(1, 1), (3, 2), (33, 3), (4000, 4), (1024 * 8 + 3, 5)])
+def test_mx_quantize_wide_range(ref, n_blocks, seed):
+    """Blocks over the whole bf16 exponent range (zeros, subnormals, the top of the
+    range, negatives), ragged counts of blocks."""
+    x = inputs.bf16_blocks_wide_range(n_blocks, seed)
+    p, s = gpu_quantize(x)
+    wp, ws = ref.mx_quantize(x)
+    assert_same_bytes(s, ws, "quantise scales")
+    assert_same_bytes(p, wp, "quantise codes")
+
+
+def test_mx_quantize_ties_specials_and_signs(ref):
+    """Hand-worked ties, saturation, +-0, Inf and NaN blocks, negatives rounding to 0."""
+    import oracle_pins
+    g = oracle_pins.golden("mx_quantize_ties.txt")
+    rows = []
+    for key in ("cases", "saturate"):
+        for pair in g[key]:
+            blk = np.zeros(32)
+            blk[0] = 6.0 if key == "cases" else 0.0
+            blk[1] = float(pair.split("=")[0])
+            rows.append(blk)
+    x = oracle_pins._bf16_bits(np.stack(rows))
+    x[len(rows) - 1, 5] = 0x8000  # -0.0
+    special = np.zeros((4, 32), np.uint16)
+    special[1, 3] = 0x7F80   # +Inf
+    special[2, 7] = 0xFFC1   # NaN
+    special[3, :] = 0x8001   # negative subnormals
+    x = np.concatenate([x, special])
+    p, s = gpu_quantize(x)
+    wp, ws = ref.mx_quantize(x)
+    assert_same_bytes(s, ws, "special scales")
+    assert_same_bytes(p, wp, "special codes")
+
+
+def test_mx_quantize_roundtrip_through_unpack(ref):
+    """GPU quantise of GPU-decoded blocks returns codes that decode to the same values."""
+    x = inputs.mx_random(64, 2880, seed=70, e_lo=2, e_hi=252, zero_fraction=True)
+    decoded = gpu_mx(x)
+    p, s = fp4.fp4_mx_quantize(decoded)
+    assert_same(bits(fp4.fp4_mx_unpack(p, s)), bits(decoded), "roundtrip")
+
+
+def test_mx_quantize_moe_full(ref):
+    """The bf16 MoE weights (normal / 10) quantised in full."""
+    for w in inputs.bf16_moe():
+        p, s = gpu_quantize(w.x)
+        wp, ws = ref.mx_quantize(w.x, threads=THREADS)
+        assert_same_bytes(s, ws, w.name + " scales")
+        assert_same_bytes(p, wp, w.name + " codes")
+
+
+@pytest.mark.parametrize("x_off,p_off", [(2, 0), (0, 1), (6, 3)])
+def test_mx_quantize_unaligned(ref, x_off, p_off):
+    """Buffers off the 16 / 4-byte boundaries take the per-block kernel: same bytes."""
+    x = inputs.bf16_blocks_wide_range(37, seed=9)
+    n = x.size
+    xbuf = torch.zeros(2 * n + 32, dtype=torch.uint8, device=DEV)
+    xbuf[x_off:x_off + 2 * n] = torch.from_numpy(x.reshape(-1).view(np.uint8)).to(DEV)
+    pbuf = torch.zeros(n // 2 + 32, dtype=torch.uint8, device=DEV)
+    sbuf = torch.zeros(n // 32 + 32, dtype=torch.uint8, device=DEV)
+    lib = fp4.load()
+    code = lib.fp4_mx_quantize(xbuf.data_ptr() + x_off, pbuf.data_ptr() + p_off, sbuf.data_ptr() + 5,
+                               37, 32, torch.cuda.current_stream().cuda_stream)
+    assert code == 0
+    wp, ws = ref.mx_quantize(x)
+    assert_same_bytes(pbuf[p_off:p_off + n // 2].cpu().numpy(), wp, "unaligned codes")
+    assert_same_bytes(sbuf[5:5 + n // 32].cpu().numpy(), ws, "unaligned scales")
+    assert int(pbuf[:p_off].sum()) == 0 and int(pbuf[p_off + n // 2:].sum()) == 0
+    assert int(sbuf[:5].sum()) == 0 and int(sbuf[5 + n // 32:].sum()) == 0
+
+
+def test_mx_quantize_errors():
+    lib = fp4.load()
+    x = torch.zeros(2, 64, dtype=torch.bfloat16, device=DEV)
+    p = torch.zeros(2, 32, dtype=torch.uint8, device=DEV)
+    s = torch.zeros(2, 2, dtype=torch.uint8, device=DEV)
+    assert lib.fp4_mx_quantize(x.data_ptr() + 1, p.data_ptr(), s.data_ptr(), 2, 64, None) == fp4.Status.ERR_ALIGN
+    assert lib.fp4_mx_quantize(x.data_ptr(), x.data_ptr() + 8, s.data_ptr(), 2, 64, None) == fp4.Status.ERR_ALIAS
+    with pytest.raises(ValueError):
+        fp4.fp4_mx_quantize(torch.zeros(2, 48, dtype=torch.bfloat16, device=DEV))

@@ -57,6 +57,20 @@ MUTATIONS = [
      "dense dequant scale row pitch wrong"),
     ("out[r * hidden + c] = nv_element(", "out[r * (hidden / 2) + c] = nv_element(",
      "dense dequant output row pitch wrong"),
+    ("shared = (e - 1) - 2;", "shared = (e - 1) - 1;", "quantise: E2M1 emax taken as 1"),
+    ("shared = (e - 1) - 2;", "shared = e - 2;", "quantise: floor(log2) off by one"),
+    ("if (err < best_err || (err == best_err && (m % 2) == 0 && (best % 2) == 1)) {",
+     "if (err <= best_err) {", "quantise: ties go up instead of to even"),
+    ("if (err < best_err || (err == best_err && (m % 2) == 0 && (best % 2) == 1)) {",
+     "if (err < best_err) {", "quantise: ties go down instead of to even"),
+    ("            if (signbit(v))\n                code |= 8u;", "",
+     "quantise: sign dropped"),
+    ("        *scale = 0xFF;", "        *scale = 0x00;", "quantise: NaN block scale wrong"),
+    ("packed16[i / 2] = (uint8_t)(codes[0] | (codes[1] << 4));",
+     "packed16[i / 2] = (uint8_t)(codes[1] | (codes[0] << 4));", "quantise: nibble order swapped"),
+    ("        if (shared < -127)\n            shared = -127;", "",
+     "quantise: scale not clamped at the smallest E8M0"),
+    ("else if (fabs(v) > amax)", "else if (v > amax)", "quantise: amax ignores negatives"),
     ("if (id < 0 || id >= vocab) {\n            for", "if (id < 0 || id > vocab) {\n            for",
      "last valid id off by one"),
 ]
