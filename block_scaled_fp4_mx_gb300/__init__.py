@@ -15,6 +15,8 @@ status raise.
 * ``fp4_mx_quantize(x_bf16)`` -- the inverse direction: bf16 -> (packed E2M1
   codes, E8M0 scales), by the OCP MX v1.0 conversion (the pages name the step,
   MXFP4QuantizeUtil.quantize, but not its rule).
+* ``fp4_mx_moe_gemm(a, expert_offsets, w_packed, w_scales)`` -- grouped MoE GEMM,
+  bf16 activations x MXFP4 expert weights decoded into the tcgen05 operand.
 * ``fp4_nv_embedding_gather(ids, weight, block_scale, global_scale)`` -- NVFP4
   embedding lookup dequantised at gather time: value * (e4m3 block scale * fp32
   global scale) in fp32, rounded to bf16 ("sgl-project/sglang pull 34222",
@@ -26,7 +28,8 @@ from __future__ import annotations
 
 from ._lib import Status, last_error, library_path, load, status_string  # noqa: F401
 
-__all__ = ["fp4_mx_unpack", "fp4_mx_quantize", "fp4_nv_embedding_gather", "fp4_nv_dequant",
+__all__ = ["fp4_mx_unpack", "fp4_mx_quantize", "fp4_mx_moe_gemm", "fp4_nv_embedding_gather",
+           "fp4_nv_dequant",
            "fp4_status_string",
            "Fp4Error",
            "Status", "load", "library_path"]
@@ -207,3 +210,40 @@ def fp4_mx_quantize(x, packed_out=None, scales_out=None, stream=None):
     if code != Status.OK:
         raise Fp4Error("fp4_mx_quantize", code)
     return packed_out, scales_out
+
+
+def fp4_mx_moe_gemm(a, expert_offsets, w_packed, w_scales, max_rows_per_expert: int,
+                    out=None, status=None, stream=None):
+    """Grouped MoE GEMM: ``a`` bf16 [T, k] (rows grouped by expert), ``expert_offsets``
+    int64 [E + 1] on the device, ``w_packed`` uint8 [E, n, k/2], ``w_scales`` uint8
+    [E, n, k/32] -> bf16 [T, n] with out[r] = a[r] @ W_e^T for r in expert e's rows.
+    ``status`` (int32 CUDA tensor, one element; allocated if None) receives
+    Status.ERR_TIMEOUT or Status.ERR_SHAPE from the device; the caller reads it after
+    synchronising. Returns (out, status)."""
+    torch = _torch()
+    _check_cuda(a, "a", (torch.bfloat16, torch.int16, torch.uint16))
+    _check_cuda(expert_offsets, "expert_offsets", (torch.int64,))
+    _check_cuda(w_packed, "w_packed", (torch.uint8,))
+    _check_cuda(w_scales, "w_scales", (torch.uint8,))
+    if a.dim() != 2 or w_packed.dim() != 3 or w_scales.dim() != 3:
+        raise ValueError("a must be [T, k], w_packed [E, n, k/2], w_scales [E, n, k/32]")
+    experts, n, half = w_packed.shape
+    k = 2 * half
+    if a.shape[1] != k or tuple(w_scales.shape) != (experts, n, k // 32):
+        raise ValueError("inconsistent k / n / expert counts")
+    if expert_offsets.numel() != experts + 1:
+        raise ValueError("expert_offsets must have experts + 1 entries")
+    if out is None:
+        out = torch.empty((a.shape[0], n), dtype=torch.bfloat16, device=a.device)
+    _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
+    if tuple(out.shape) != (a.shape[0], n):
+        raise ValueError(f"out must have shape {(a.shape[0], n)}")
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=a.device)
+    _check_cuda(status, "status", (torch.int32,))
+    code = load().fp4_mx_moe_gemm(_ptr(a), _ptr(expert_offsets), experts, int(max_rows_per_expert),
+                                  _ptr(w_packed), _ptr(w_scales), n, k, a.shape[0], _ptr(out),
+                                  _ptr(status), _stream_handle(stream, a.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_mx_moe_gemm", code)
+    return out, status

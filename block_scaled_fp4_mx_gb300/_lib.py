@@ -28,6 +28,7 @@ class Status(enum.IntEnum):
     ERR_POINTER = 7
     ERR_ALIAS = 8
     ERR_ALIGN = 9
+    ERR_TIMEOUT = 10
 
 
 # Every function the header declares, with its ctypes signature.
@@ -39,6 +40,8 @@ SIGNATURES = {
                                 ctypes.c_int),
     "fp4_nv_dequant": ([_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp], ctypes.c_int),
     "fp4_mx_quantize": ([_vp, _vp, _vp, _i64, _i64, _vp], ctypes.c_int),
+    "fp4_mx_moe_gemm": ([_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp],
+                        ctypes.c_int),
     "fp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "fp4_last_error": ([], ctypes.c_char_p),
     "fp4_abi_version": ([], ctypes.c_int),

@@ -193,6 +193,45 @@ FP4_EXPORT fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_o
     return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_quantize launch");
 }
 
+FP4_EXPORT fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *expert_offsets,
+                                      int64_t experts, int64_t max_rows_per_expert,
+                                      const uint8_t *w_packed, const uint8_t *w_scales_e8m0,
+                                      int64_t n, int64_t k, int64_t total_rows,
+                                      uint16_t *out_bf16, int32_t *status,
+                                      fp4_stream_t stream) {
+    clear_error();
+    if (experts < 0 || max_rows_per_expert < 0 || n < 0 || k < 0 || total_rows < 0)
+        return FP4_ERR_SHAPE;
+    if (k % 32 != 0 || n % 32 != 0) return FP4_ERR_SHAPE;
+    if (experts > 65535 || max_rows_per_expert > 65535ll * 128 || n > (1ll << 30) ||
+        k > (1ll << 30))
+        return FP4_ERR_SHAPE;
+    if (experts == 0 || max_rows_per_expert == 0 || n == 0) return FP4_OK;
+    if (a_bf16 == nullptr || expert_offsets == nullptr || w_packed == nullptr ||
+        w_scales_e8m0 == nullptr || out_bf16 == nullptr || status == nullptr)
+        return FP4_ERR_NULL_PTR;
+    if (k == 0) return FP4_ERR_SHAPE;  // an empty reduction: nothing to multiply
+    if (misaligned(a_bf16, 16) || misaligned(w_packed, 4) || misaligned(out_bf16, 16) ||
+        misaligned(expert_offsets, 8) || misaligned(status, 4))
+        return FP4_ERR_ALIGN;
+    const uint64_t out_bytes = (uint64_t)total_rows * (uint64_t)n * 2;
+    const uint64_t w_bytes = (uint64_t)experts * (uint64_t)n * (uint64_t)k / 2;
+    if (overlaps(out_bf16, out_bytes, a_bf16, (uint64_t)total_rows * (uint64_t)k * 2) ||
+        overlaps(out_bf16, out_bytes, w_packed, w_bytes) ||
+        overlaps(out_bf16, out_bytes, w_scales_e8m0, w_bytes / 16) ||
+        overlaps(out_bf16, out_bytes, expert_offsets, (uint64_t)(experts + 1) * 8) ||
+        overlaps(out_bf16, out_bytes, status, 4))
+        return FP4_ERR_ALIAS;
+    const void *ptrs[] = {a_bf16, expert_offsets, w_packed, w_scales_e8m0, out_bf16, status};
+    const fp4_status s = check_pointers(ptrs, 6);
+    if (s != FP4_OK) return s;
+    const cudaError_t err = fp4mx::launch_mx_moe_gemm(a_bf16, expert_offsets, experts,
+                                                      max_rows_per_expert, total_rows, w_packed,
+                                                      w_scales_e8m0, n, k, out_bf16, status,
+                                                      (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_moe_gemm launch");
+}
+
 FP4_EXPORT fp4_status fp4_nv_dequant(const uint8_t *weight, const uint8_t *block_scale_e4m3,
                                      const float *global_scale, int64_t rows, int64_t hidden,
                                      int64_t group_size, uint16_t *out_bf16,
@@ -232,10 +271,11 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
     case FP4_ERR_POINTER: return "pointer is not device-accessible CUDA memory";
     case FP4_ERR_ALIAS: return "output overlaps an input";
     case FP4_ERR_ALIGN: return "pointer not aligned to its element type";
+    case FP4_ERR_TIMEOUT: return "a bounded wait on the tensor core ran out (reported in status)";
     }
     return "unknown status";
 }
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 102; }
+FP4_EXPORT int fp4_abi_version(void) { return 103; }

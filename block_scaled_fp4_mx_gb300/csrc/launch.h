@@ -28,6 +28,12 @@ cudaError_t launch_nv_dequant(const uint8_t *weight, const uint8_t *scales,
 cudaError_t launch_mx_quantize(const uint16_t *in, uint8_t *packed, uint8_t *scales,
                                int64_t n_elems, cudaStream_t stream);
 
+// Grouped MoE GEMM with MXFP4 weights decoded into the tensor-core B operand.
+cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets, int64_t experts,
+                               int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
+                               const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
+                               int32_t *status, cudaStream_t stream);
+
 // Resident CTAs per SM x SM count for `kernel` at `threads` threads, cached per
 // device; a grid no larger than this runs in one wave.
 int max_resident_ctas(const void *kernel, int threads, int slot);

@@ -2,7 +2,7 @@
  * fp4mx.h -- C ABI of a GB300 (sm_103a) library that decodes block-scaled FP4
  * (E2M1) data into bf16.
  *
- * Four operations, each one CUDA kernel launch on the caller's stream:
+ * Five operations, each one CUDA kernel launch on the caller's stream:
  *
  *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
  *                             a wrapping 16-bit integer add into the bf16 exponent
@@ -13,6 +13,8 @@
  *                             in fp32 and rounded to bf16 (nearest, ties to even).
  *   fp4_nv_dequant            the same NVFP4 decode over every row of a table.
  *   fp4_mx_quantize           bf16 to MXFP4 (the inverse direction of the unpack).
+ *   fp4_mx_moe_gemm           grouped MoE GEMM, MXFP4 weights decoded into the
+ *                             tensor-core operand (tcgen05), bf16 activations.
  *
  * Conventions shared by every entry point:
  *   - Pointers named "device" must be device-accessible CUDA allocations
@@ -58,7 +60,8 @@ typedef enum fp4_status {
     FP4_ERR_CUDA = 6,        /* the CUDA runtime reported an error (see fp4_last_error) */
     FP4_ERR_POINTER = 7,     /* a pointer is not device-accessible memory           */
     FP4_ERR_ALIAS = 8,       /* an output range overlaps an input range             */
-    FP4_ERR_ALIGN = 9        /* a uint16/int32/int64/float pointer not aligned to its type */
+    FP4_ERR_ALIGN = 9,       /* a pointer not aligned as its entry point requires   */
+    FP4_ERR_TIMEOUT = 10     /* written to a status word: a bounded device wait ran out */
 } fp4_status;
 
 /*
@@ -149,6 +152,46 @@ fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_out, uint8_t
                            int64_t rows, int64_t k, fp4_stream_t stream);
 
 /*
+ * fp4_mx_moe_gemm -- grouped MoE expert GEMM with MXFP4 weights, the decode fused
+ * into the tensor-core operand (tcgen05 on sm_103a).
+ *
+ * The consumer of the MXFP4 unpack on the pages: "vllm-project/vllm pull 51583"
+ * (prhub digest), "Motivation" and the comments on the unpack_B loop -- the CPU
+ * MoE GEMM unpacks each tile of MXFP4 expert weights to bf16 before multiplying.
+ * For expert e with activation rows [offsets[e], offsets[e+1]):
+ *     out[r][j] = sum_k a[r][k] * W_e[j][k]        (r in expert e's rows, j < n)
+ * where W_e[j][k] is the bf16 value fp4_mx_unpack gives for row j of expert e's
+ * packed weights. Products and sums are accumulated in fp32 by the tensor core
+ * (summation order unspecified), then rounded to bf16 (nearest, ties to even).
+ *
+ *   a_bf16               device, uint16[total_rows * k] bf16 bits, row-major, the rows
+ *                        of each expert contiguous; 16-byte aligned
+ *   expert_offsets       device, int64[experts + 1], non-decreasing, offsets[0] = 0,
+ *                        offsets[experts] = total_rows
+ *   experts              number of experts (<= 65535)
+ *   max_rows_per_expert  upper bound on offsets[e+1] - offsets[e] (sets the grid; an
+ *                        expert with more rows is not computed and status is set to
+ *                        FP4_ERR_SHAPE)
+ *   w_packed             device, uint8[experts * n * k / 2]: expert e's [n, k/2] codes
+ *                        (as fp4_mx_unpack reads them); 4-byte aligned
+ *   w_scales_e8m0        device, uint8[experts * n * k / 32]
+ *   n, k                 output columns and reduction length, both multiples of 32
+ *   total_rows           rows of a and out; an expert whose rows fall outside
+ *                        [0, total_rows) is not computed and status is set to
+ *                        FP4_ERR_SHAPE (the offsets are checked on the device)
+ *   out_bf16             device, uint16[total_rows * n], row-major; 16-byte aligned
+ *   status               device int32, required. Set to FP4_ERR_TIMEOUT if a bounded
+ *                        wait on the tensor core ran out (the kernel then stops, frees
+ *                        its tensor memory and returns) or FP4_ERR_SHAPE as above;
+ *                        never cleared by the library.
+ *   stream               CUDA stream the kernel is enqueued on
+ */
+fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *expert_offsets, int64_t experts,
+                           int64_t max_rows_per_expert, const uint8_t *w_packed,
+                           const uint8_t *w_scales_e8m0, int64_t n, int64_t k, int64_t total_rows,
+                           uint16_t *out_bf16, int32_t *status, fp4_stream_t stream);
+
+/*
  * fp4_nv_dequant -- dequantise a whole NVFP4 table (every row, in order).
  *
  * The dense counterpart of fp4_nv_embedding_gather: out[r][c] is what the
@@ -179,7 +222,7 @@ const char *fp4_status_string(fp4_status status);
 const char *fp4_last_error(void);
 
 /* Version of this ABI (major * 100 + minor): 101 adds fp4_nv_dequant, 102 adds
- * fp4_mx_quantize and FP4_ERR_ALIGN. */
+ * fp4_mx_quantize and FP4_ERR_ALIGN, 103 adds fp4_mx_moe_gemm and FP4_ERR_TIMEOUT. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

@@ -19,6 +19,10 @@ Functions and the passages they follow (web pages cited by title and section):
 * ``e4m3_to_f32``, ``f32_to_bf16_rne``, ``e2m1_bf16_bits`` -- the element
   conversions those steps use (OCP FP8 E4M3 definition; IEEE round to nearest
   even into bf16; the E2M1 codebook).
+* ``mx_moe_gemm`` -- the grouped MoE GEMM the unpack feeds ("vllm-project/vllm
+  pull 51583", the unpack_B loop of the CPU MoE GEMM): per expert, activations
+  times the unpacked weights transposed, exact in float64 (numpy matmul as the
+  step), with the sum of |a||w| that bounds fp32 accumulation error.
 * ``nv_dequant`` -- the same NVFP4 element rule over every row of a table (the
   dense dequant a tied lm_head needs; same page, "Comments" and "Risks").
 * ``nv_embedding_gather`` / ``nv_embedding_gather_at`` -- NVFP4 gather-dequant,
@@ -202,6 +206,32 @@ class Oracle:
                                     int(threads))
         return (packed.reshape(*shape[:-1], shape[-1] // 2),
                 scales.reshape(*shape[:-1], shape[-1] // 32))
+
+    def bf16_to_f64(self, bits) -> np.ndarray:
+        """Exact float64 values of bf16 bit patterns (bf16 is the top half of fp32)."""
+        b = np.ascontiguousarray(bits, dtype=np.uint16)
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    def mx_moe_gemm(self, a_bits, offsets, w_packed, w_scales, threads: int = 1):
+        """Grouped MoE GEMM, exact in float64: for expert e and its rows
+        [offsets[e], offsets[e+1]) of ``a`` (bf16 bits [T, k]),
+        out = a_rows @ W_e^T with W_e the MXFP4 unpack of expert e's weights
+        ([n, k/2] codes, [n, k/32] E8M0). The products of two bf16 values are exact in
+        float64 and the float64 sums are far more precise than the fp32 accumulation
+        they are compared with. Returns (out, sum of |a||w| per output element)."""
+        a = self.bf16_to_f64(a_bits)
+        offsets = np.asarray(offsets, dtype=np.int64)
+        experts, n, half = w_packed.shape
+        out = np.zeros((a.shape[0], n))
+        absdot = np.zeros((a.shape[0], n))
+        for e in range(experts):
+            r0, r1 = int(offsets[e]), int(offsets[e + 1])
+            if r1 <= r0:
+                continue
+            w = self.bf16_to_f64(self.mx_unpack(w_packed[e], w_scales[e], threads)).reshape(n, 2 * half)
+            out[r0:r1] = a[r0:r1] @ w.T
+            absdot[r0:r1] = np.abs(a[r0:r1]) @ np.abs(w).T
+        return out, absdot
 
     # -- NVFP4 ----------------------------------------------------------------
     def nv_embedding_gather(self, ids, weight, scales, global_scale, group_size: int = 16,

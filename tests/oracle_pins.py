@@ -376,6 +376,65 @@ def pin_mx_quantize_error_bound(o):
 
 
 # ---------------------------------------------------------------------------
+# pins: grouped MoE GEMM (activations x unpacked weights)
+# ---------------------------------------------------------------------------
+
+def _diag_weights(experts, n, k, e8m0_of_expert):
+    """Packed weights whose unpack is 2^(E_e - 127) on the diagonal (code 2 = 1.0)
+    and 0 elsewhere."""
+    codes = np.zeros((experts, n, k), dtype=np.uint8)
+    for j in range(min(n, k)):
+        codes[:, j, j] = 2
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    scales = np.zeros((experts, n, k // 32), dtype=np.uint8)
+    for e in range(experts):
+        scales[e] = e8m0_of_expert(e)
+    return packed, scales
+
+
+def pin_moe_gemm_routes_rows_to_their_expert(o):
+    """With expert e's weights 2^e times the identity, each row comes out as its own
+    first n values times 2^e of the expert that owns it (empty experts included)."""
+    rng = np.random.default_rng(81)
+    k, n = 64, 32
+    offsets = np.array([0, 3, 3, 10, 11])
+    a_bits = _bf16_bits(rng.standard_normal((11, k)))
+    packed, scales = _diag_weights(4, n, k, lambda e: 127 + e)
+    out, _ = o.mx_moe_gemm(a_bits, offsets, packed, scales)
+    a = o.bf16_to_f64(a_bits)
+    for e in range(4):
+        r0, r1 = offsets[e], offsets[e + 1]
+        assert np.array_equal(out[r0:r1], a[r0:r1, :n] * 2.0 ** e)
+
+
+def pin_moe_gemm_brute_force(o):
+    """Small grouped GEMM against a plain triple loop over the decoded values
+    (values are dyadic with few bits, so every sum is exact in either order)."""
+    rng = np.random.default_rng(82)
+    k, n, experts = 64, 32, 2
+    offsets = np.array([0, 2, 5])
+    a_vals = rng.integers(-8, 9, size=(5, k)) / 4.0
+    a_bits = _bf16_bits(a_vals)
+    x = inputs.mx_random(experts * n, k, seed=83, e_lo=125, e_hi=129)
+    packed = x.packed.reshape(experts, n, k // 2)
+    scales = x.scales.reshape(experts, n, k // 32)
+    out, absdot = o.mx_moe_gemm(a_bits, offsets, packed, scales)
+    codes = nibble_codes(x.packed).reshape(experts, n, k)
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for e in range(experts):
+        for r in range(offsets[e], offsets[e + 1]):
+            for j in range(n):
+                acc = 0.0
+                acc_abs = 0.0
+                for kk in range(k):
+                    c = int(codes[e, j, kk])
+                    wv = (-1.0 if c & 8 else 1.0) * mags[c & 7] * 2.0 ** (int(scales[e, j, kk // 32]) - 127)
+                    acc += a_vals[r, kk] * wv
+                    acc_abs += abs(a_vals[r, kk] * wv)
+                assert out[r, j] == acc and absdot[r, j] == acc_abs, (e, r, j)
+
+
+# ---------------------------------------------------------------------------
 # pins: NVFP4
 # ---------------------------------------------------------------------------
 

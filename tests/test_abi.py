@@ -52,10 +52,10 @@ def test_only_api_symbols_exported():
 
 def test_status_strings(lib):
     assert fp4.fp4_status_string(0) == "ok"
-    for code in range(1, 10):
+    for code in range(1, 11):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 102
+    assert lib.fp4_abi_version() == 103
 
 
 def test_mx_host_validation(lib):
@@ -125,6 +125,21 @@ def test_alignment_refused_before_cuda(lib):
     assert g(base, base + 16000, base + 20001) == fp4.Status.ERR_ALIGN
     assert lib.fp4_nv_dequant(base + 8192, base + 12288, base + 16001, 4, 64, 16, base + 20000,
                               None) == fp4.Status.ERR_ALIGN
+
+
+def test_moe_gemm_host_validation(lib):
+    f = lib.fp4_mx_moe_gemm
+    g = lambda e, mr, n, k, ptr=None: f(ptr, ptr, e, mr, ptr, ptr, n, k, 8, ptr, ptr, None)
+    assert g(1, 8, 64, 48) == fp4.Status.ERR_SHAPE       # k % 32
+    assert g(1, 8, 48, 64) == fp4.Status.ERR_SHAPE       # n % 32
+    assert g(70000, 8, 64, 64) == fp4.Status.ERR_SHAPE   # experts > 65535
+    assert g(0, 8, 64, 64) == fp4.Status.OK
+    assert g(1, 0, 64, 64) == fp4.Status.OK
+    assert g(1, 8, 64, 64) == fp4.Status.ERR_NULL_PTR
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = ctypes.addressof(buf)
+    base += (-base) % 16
+    assert f(base + 8, base, 1, 8, base, base, 64, 64, 8, base, base, None) == fp4.Status.ERR_ALIGN
 
 
 def test_binding_refuses_cpu_tensors():

@@ -1,0 +1,113 @@
+"""GPU parity of the grouped MoE GEMM (MXFP4 weights decoded into the tcgen05 operand).
+
+The oracle is exact (float64 sums of exact bf16 x bf16 products). The GPU sums in
+fp32 inside the tensor core, in an order it does not specify, then rounds to bf16,
+so the comparison takes the bound of that arithmetic: with S = sum_k |a_k w_k|,
+|fp32 sum - exact| <= K * 2^-23 * S (twice the textbook gamma_K = K * 2^-24, which
+leaves room for adders that truncate), and the bf16 rounding adds at most 2^-8 of
+the magnitude. A dropped K-slice, a swapped operand, a wrong scale or a wrong row
+of weights is orders of magnitude outside it.
+"""
+import numpy as np
+import pytest
+
+import block_scaled_fp4_mx_gb300 as fp4
+from block_scaled_fp4_mx_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def tolerance(exact, absdot, k):
+    return 2.0 ** -8 * np.abs(exact) + (1 + 2.0 ** -8) * k * 2.0 ** -23 * absdot
+
+
+def run_case(ref, rows, n, k, seed, e_lo=118, e_hi=132, max_rows=None, a_scale=1.0):
+    experts = len(rows)
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    total = int(offsets[-1])
+    rng = np.random.default_rng(seed)
+    a_bits = inputs.bf16_normal_bits(rng, max(total, 1) * k, scale=a_scale)[: total * k].reshape(total, k)
+    w = inputs.mx_random(experts * n, k, seed + 1, e_lo=e_lo, e_hi=e_hi, zero_fraction=True)
+    packed = w.packed.reshape(experts, n, k // 2)
+    scales = w.scales.reshape(experts, n, k // 32)
+    a_t = torch.from_numpy(a_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    out, status = fp4.fp4_mx_moe_gemm(
+        a_t, torch.from_numpy(offsets).to(DEV), torch.from_numpy(packed).to(DEV),
+        torch.from_numpy(scales).to(DEV), max(rows) if max_rows is None else max_rows)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    got = out.float().cpu().numpy().astype(np.float64)
+    exact, absdot = ref.mx_moe_gemm(a_bits, offsets, packed, scales, threads=ref.max_threads())
+    err = np.abs(got - exact)
+    tol = tolerance(exact, absdot, k)
+    bad = err > tol
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{int(bad.sum())} of {bad.size} outside the bound; first {tuple(i)}: "
+                             f"gpu {got[tuple(i)]} exact {exact[tuple(i)]} tol {tol[tuple(i)]}")
+    return got, exact
+
+
+def test_single_tile(oracle_impl):
+    """One expert, one 128 x 128 tile, one 64-wide K slice (four MMAs)."""
+    run_case(oracle_impl, [128], 128, 64, seed=1)
+
+
+def test_k_loop_and_tiles(oracle_impl):
+    """Several K slices, several row and column tiles."""
+    run_case(oracle_impl, [256], 256, 512, seed=2)
+
+
+@pytest.mark.parametrize("rows,n,k", [([1], 32, 32), ([77], 96, 2880), ([130, 5], 160, 96),
+                                      ([0, 200, 3, 0, 128], 2880 // 2, 256)])
+def test_ragged_shapes(oracle_impl, rows, n, k):
+    """Ragged rows per expert (including empty experts), n and k that are not
+    multiples of the 128 x 64 tile."""
+    run_case(oracle_impl, rows, n, k, seed=sum(rows) + n + k)
+
+
+def test_identity_weights_exact(oracle_impl):
+    """Weights 2^e * identity for expert e: the product is exact, so the bf16 output
+    must equal the activations times 2^e bit for bit."""
+    import oracle_pins
+    k, n = 128, 128
+    rows = [64, 0, 70]
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    rng = np.random.default_rng(5)
+    a_bits = oracle_pins._bf16_bits(rng.standard_normal((134, k)))
+    packed, scales = oracle_pins._diag_weights(3, n, k, lambda e: 127 + e)
+    out, status = fp4.fp4_mx_moe_gemm(
+        torch.from_numpy(a_bits.view(np.int16)).to(DEV).view(torch.bfloat16),
+        torch.from_numpy(offsets).to(DEV), torch.from_numpy(packed).to(DEV),
+        torch.from_numpy(scales).to(DEV), 70)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    exact, _ = oracle_impl.mx_moe_gemm(a_bits, offsets, packed, scales)
+    assert np.array_equal(got, oracle_pins._bf16_bits(exact))
+
+
+def test_moe_gate_up_shape(oracle_impl):
+    """32 experts x 128 tokens against the gate+up weights [32, 5760, 2880]."""
+    run_case(oracle_impl, [128] * 32, 5760, 2880, seed=7)
+
+
+def test_rows_beyond_capacity_flagged(oracle_impl):
+    """An expert with more rows than max_rows_per_expert is not computed and the
+    status word says FP4_ERR_SHAPE."""
+    k, n = 64, 64
+    offsets = torch.tensor([0, 10, 300], dtype=torch.int64, device=DEV)
+    a = torch.zeros(300, k, dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros(2, n, k // 2, dtype=torch.uint8, device=DEV)
+    s = torch.full((2, n, k // 32), 127, dtype=torch.uint8, device=DEV)
+    _, status = fp4.fp4_mx_moe_gemm(a, offsets, w, s, 128)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fp4.Status.ERR_SHAPE
