@@ -48,7 +48,8 @@ METRIC = "decoded FP4 elements/sec and achieved HBM GB/s (% of GB300 peak), 1 GP
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("step", "mx_moe", "mx_stress", "mx_exhaustive", "nv_embedding_200k",
-             "nv_embedding_32k", "nv_dequant_200k", "nv_dequant_32k", "mx_quantize_moe")
+             "nv_embedding_32k", "nv_dequant_200k", "nv_dequant_32k", "mx_quantize_moe",
+             "mx_moe_gemm_128", "mx_moe_gemm_512")
 
 
 # ---------------------------------------------------------------------------
@@ -365,6 +366,71 @@ class MxQuantOp:
         return f"rows of {self.w.name}"
 
 
+class MoeGemmOp:
+    """fp4_mx_moe_gemm: bf16 activations grouped by expert x MXFP4 expert weights."""
+    kind, kernel = "mx_moe_gemm", "mx_moe_gemm_kernel"
+
+    def __init__(self, w, rows_per_expert: int, seed: int = 6):
+        from block_scaled_fp4_mx_gb300 import inputs
+        self.experts = 32
+        self.n = w.rows // self.experts
+        self.k = w.k
+        self.w = w
+        self.rows = rows_per_expert
+        t = self.experts * rows_per_expert
+        self.a_bits = inputs.bf16_normal_bits(np.random.default_rng(seed), t * self.k,
+                                              scale=1.0).reshape(t, self.k)
+        self.offsets = np.arange(self.experts + 1, dtype=np.int64) * rows_per_expert
+        self.elems = w.n_elems  # weights decoded per launch
+        self.flops = 2.0 * t * self.n * self.k
+        self.bytes = w.packed.size + w.scales.size + 2 * t * self.k + 2 * t * self.n
+        self.min_bytes = self.bytes
+        self.units, self.elems_per_unit = self.experts, self.n * self.k
+
+    def to_device(self, torch, dev):
+        self.a = torch.from_numpy(self.a_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.off = torch.from_numpy(self.offsets).to(dev)
+        self.wp = torch.from_numpy(self.w.packed.reshape(self.experts, self.n, self.k // 2)).to(dev)
+        self.ws = torch.from_numpy(self.w.scales.reshape(self.experts, self.n, self.k // 32)).to(dev)
+        self.o = torch.empty(self.a.shape[0], self.n, dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch(self, fp4, stream):
+        fp4.fp4_mx_moe_gemm(self.a, self.off, self.wp, self.ws, self.rows, out=self.o,
+                            status=self.status, stream=stream)
+
+    def unfused(self, torch, fp4, stream):
+        """The two-step path for comparison: fp4_mx_unpack of all expert weights to
+        bf16 in HBM, then a cuBLAS batched bf16 GEMM."""
+        if not hasattr(self, "w_bf16"):
+            self.w_bf16 = torch.empty(self.experts, self.n, self.k, dtype=torch.bfloat16,
+                                      device=self.a.device)
+        fp4.fp4_mx_unpack(self.wp, self.ws, out=self.w_bf16.view(self.experts, self.n, self.k),
+                          stream=stream)
+        a3 = self.a.view(self.experts, self.rows, self.k)
+        torch.bmm(a3, self.w_bf16.transpose(1, 2), out=self.o.view(self.experts, self.rows, self.n))
+
+    def e2e_jobs(self, torch, fp4, chunks):
+        ha = torch.from_numpy(self.a_bits.view(np.int16)).pin_memory().view(torch.bfloat16)
+        ho = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+
+        def fn(st):
+            self.a.copy_(ha, non_blocking=True)
+            fp4.fp4_mx_moe_gemm(self.a, self.off, self.wp, self.ws, self.rows, out=self.o,
+                                status=self.status, stream=st)
+            ho.copy_(self.o, non_blocking=True)
+        return [(ha.numel() * 2, ho.numel() * 2, fn)]
+
+    def oracle_units(self, o, n, threads):
+        r = n * self.rows
+        o.mx_moe_gemm(self.a_bits[:r], self.offsets[:n + 1],
+                      self.w.packed.reshape(self.experts, self.n, self.k // 2)[:n],
+                      self.w.scales.reshape(self.experts, self.n, self.k // 32)[:n], threads)
+
+    def sample_name(self):
+        return f"experts of the MoE GEMM ({self.rows} tokens each)"
+
+
 def load_workload(name: str):
     """The ops of one step of the named workload, in launch order."""
     from block_scaled_fp4_mx_gb300 import inputs
@@ -379,6 +445,8 @@ def load_workload(name: str):
         "nv_dequant_200k": lambda: [NvDenseOp(inputs.nv_embedding_200k())],
         "nv_dequant_32k": lambda: [NvDenseOp(inputs.nv_embedding_32k())],
         "mx_quantize_moe": lambda: [MxQuantOp(w) for w in inputs.bf16_moe()],
+        "mx_moe_gemm_128": lambda: [MoeGemmOp(inputs.mx_moe()[0], 128)],
+        "mx_moe_gemm_512": lambda: [MoeGemmOp(inputs.mx_moe()[0], 512)],
     }
     return table[name]()
 
@@ -398,6 +466,16 @@ def measured_peak():
         return float(peaks["hbm_gbs"]), "measured"
     except Exception:  # noqa: BLE001
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            peaks = json.load(fh)
+        return float(peaks["bf16_tflops"]), "measured"
+    except Exception:  # noqa: BLE001
+        return 1900.0, "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -481,13 +559,15 @@ def run_ours(args, d: Dist):
     value = step_elems * k * d.world / (elapsed_ms / 1e3)
     alg_gbs = step_bytes * k / (elapsed_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
+    tensor_peak, tensor_kind = measured_tensor_peak()
 
     # per kernel kind: summed bytes and durations of its launches
     kernels = {}
     for i, op in enumerate(ops):
         ms = sum(ev[i][0].elapsed_time(ev[i][1]) for ev in events)
         kk = kernels.setdefault(op.kind, {"kernel": op.kernel, "launches_per_step": 0, "ms": 0.0,
-                                          "elements": 0, "bytes": 0, "min_bytes": 0})
+                                          "elements": 0, "bytes": 0, "min_bytes": 0, "flops": 0.0})
+        kk["flops"] += getattr(op, "flops", 0.0)
         kk["launches_per_step"] += 1
         kk["ms"] += ms
         kk["elements"] += op.elems
@@ -503,7 +583,10 @@ def run_ours(args, d: Dist):
         if kk["min_bytes"] != kk["bytes"]:
             kk["distinct_row_bytes_per_launch"] = kk["min_bytes"] / n
             kk["gbs_distinct_rows"] = kk["min_bytes"] / n / launch_s / 1e9
-        for key in ("elements", "bytes", "min_bytes"):
+        if kk["flops"]:
+            kk["tflops"] = kk["flops"] / n / launch_s / 1e12
+            kk["frac_of_tensor_peak"] = kk["tflops"] / tensor_peak
+        for key in ("elements", "bytes", "min_bytes", "flops"):
             kk.pop(key)
     dominant = max(kernels, key=lambda kind: kernels[kind]["avg_launch_us"]
                    * kernels[kind]["launches_per_step"])
@@ -514,6 +597,35 @@ def run_ours(args, d: Dist):
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "traffic": traffic, "traffic_source": capture}
+    if "tflops" in dk:
+        roofline.update(bound="tensor", achieved=dk["tflops"], peak=tensor_peak, unit="TFLOP/s",
+                        frac=dk["tflops"] / tensor_peak,
+                        peak_source="measured dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                        if tensor_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
+                        hbm_gbs=dk["gbs"], hbm_frac=dk["gbs"] / peak)
+
+    comparison = None
+    if all(hasattr(op, "unfused") for op in ops):
+        for _ in range(3):
+            for op in ops:
+                op.unfused(torch, fp4, stream)
+        c0, c1 = mk()
+        torch.cuda.synchronize()
+        c0.record(stream)
+        for _ in range(max(1, min(k, 50))):
+            for op in ops:
+                op.unfused(torch, fp4, stream)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        ms_unfused = c0.elapsed_time(c1) / max(1, min(k, 50))
+        comparison = {"unfused_ms_per_step": ms_unfused,
+                      "fused_ms_per_step": elapsed_ms / k,
+                      "speedup": ms_unfused / (elapsed_ms / k),
+                      "what": "fp4_mx_unpack of the weights to bf16 + cuBLAS batched bf16 GEMM "
+                              "(torch.bmm), same inputs"}
+        for op in ops:
+            op.launch(fp4, stream)  # leave the fused result in place
+        torch.cuda.synchronize()
 
     e2e = None if args.no_e2e else run_e2e(args, d, dev, ops, step_elems)
     cpu = None
@@ -537,6 +649,7 @@ def run_ours(args, d: Dist):
                    "parallelism": f"replicas x{d.world}"},
         "hbm_gbs_algorithmic": alg_gbs, "pct_of_peak_hbm": 100.0 * alg_gbs / peak,
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        **({"comparison": comparison} if comparison else {}),
         "gpu_launches": len(ops) * k, "clocks": sampler.summary(t0, t1),
         "device": torch.cuda.get_device_name(dev),
     }

@@ -211,7 +211,7 @@ FP4_EXPORT fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *exp
         w_scales_e8m0 == nullptr || out_bf16 == nullptr || status == nullptr)
         return FP4_ERR_NULL_PTR;
     if (k == 0) return FP4_ERR_SHAPE;  // an empty reduction: nothing to multiply
-    if (misaligned(a_bf16, 16) || misaligned(w_packed, 4) || misaligned(out_bf16, 16) ||
+    if (misaligned(a_bf16, 16) || misaligned(w_packed, 16) || misaligned(out_bf16, 16) ||
         misaligned(expert_offsets, 8) || misaligned(status, 4))
         return FP4_ERR_ALIGN;
     const uint64_t out_bytes = (uint64_t)total_rows * (uint64_t)n * 2;

@@ -4,18 +4,28 @@
 // The consumer the pages' unpack serves: "vllm-project/vllm pull 51583",
 // "Motivation" and the comments on the unpack_B loop -- the CPU MoE GEMM
 // (ops.fused_experts_cpu with CPUQuantMethod.MXFP4) unpacks a tile of MXFP4
-// weights to bf16 and multiplies it with bf16 activations. Here one CTA owns a
-// 128 x 128 output tile of one expert: for every 64-wide slice of K it decodes
-// the expert's 128 x 64 weight tile (MXFP4 rule of fp4_mx_unpack, in registers)
-// straight into shared memory in the 128-byte-swizzled K-major layout the
-// tensor core reads, stages the matching 128 x 64 bf16 activation tile beside
-// it, and one thread issues four tcgen05.mma kind::f16 (M = 128, N = 128,
-// K = 16 each) accumulating in fp32 in tensor memory. The bf16 weights never
-// reach HBM: 0.53 bytes per weight are read instead of 2.
+// weights to bf16 and multiplies it with bf16 activations. Here the bf16 weights
+// never reach HBM: 0.53 bytes per weight are read instead of 2.
 //
-// Every wait on an mbarrier is bounded: if the tensor core does not signal
-// completion within kWaitLimit polls the kernel records FP4_ERR_TIMEOUT in the
-// caller's status word, stops issuing work, frees its tensor memory and returns.
+// One CTA owns a 128 x 128 output tile of one expert and runs a kStages-deep
+// shared-memory ring over 64-wide slices of K, with three roles:
+//   - the TMA engine loads each 128 x 64 bf16 activation tile (one thread issues
+//     cp.async.bulk.tensor with the 128-byte swizzle the tensor core reads);
+//   - 8 decoder warps turn the expert's 128 x 64 MXFP4 weight tile into bf16 in
+//     the same swizzled K-major layout: each thread takes one row's 32 codes of
+//     the slice (one 16-byte load, one E8M0 byte, one scaled table), decoded in
+//     registers, with the raw words of the next two slices already in flight;
+//   - one thread of the MMA warp waits for a full stage, issues four
+//     tcgen05.mma kind::f16 (M = 128, N = 128, K = 16) into the fp32 accumulator
+//     in tensor memory and commits the stage back to its "empty" barrier.
+// The decoder warps then read the accumulator with tcgen05.ld, round to bf16
+// and store the tile.
+//
+// Every wait on an mbarrier is bounded: a wait that runs out records
+// FP4_ERR_TIMEOUT in the caller's status word and sets a shared abort flag; all
+// roles then stop issuing work, the tensor memory is freed and the CTA returns.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
+
 #include "fp4_decode.cuh"
 #include "fp4mx.h"
 #include "launch.h"
@@ -23,17 +33,22 @@
 namespace fp4mx {
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps: one per 32-lane quarter of tensor memory
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 constexpr int kTileK = 64;  // one 128-byte swizzle atom of bf16 along K
+constexpr int kStages = 3;
+constexpr int kDecodeWarps = 8;  // 2 threads per weight row: 256 threads
+constexpr int kMmaWarp = kDecodeWarps;
+constexpr int kThreads = (kDecodeWarps + 1) * 32;
+constexpr int kDecodeThreads = kDecodeWarps * 32;
 constexpr uint32_t kTmemCols = 128;  // fp32 accumulator: one column per output column
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kTileBytes = kTileM * kTileK * 2;  // 16 KiB per operand tile
-// shared memory: A tile, B tile, then the mbarrier, tensor-memory address and
-// abort flag; +1 KiB to align the tiles to the 1024-byte swizzle atom, padded so
-// that at most 4 CTAs (4 x 128 tensor-memory columns) share an SM.
-constexpr int kSmemBytes = 56 * 1024;
+constexpr int kTileBytes = kTileM * kTileK * 2;  // 16 KiB per operand tile and stage
+// shared memory: 1 KiB to align the tiles to the 1024-byte swizzle atom, the A
+// and B rings, then barriers, the tensor-memory address and the abort flag.
+// Two CTAs (2 x 128 tensor-memory columns) fit on an SM.
+constexpr int kBarrierOffset = 2 * kStages * kTileBytes;
+constexpr int kSmemBytes = 1024 + kBarrierOffset + 256;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -123,18 +138,48 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t kc) {
     return r * 128u + ((kc ^ (r & 7u)) << 4);
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// TMA: 2-D tile (x = K offset in elements, y = row) of the tensor map into shared
+// memory, completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+struct RawSlice {
+    uint4 words;  // 32 packed codes of one weight row (4 words)
+    uint32_t e8m0;
+};
+
 __global__ void __launch_bounds__(kThreads)
-mx_moe_gemm_kernel(const uint16_t *__restrict__ a, const int64_t *__restrict__ expert_offsets,
+mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const int64_t *__restrict__ expert_offsets,
                    const uint8_t *__restrict__ w_packed, const uint8_t *__restrict__ w_scales,
                    int64_t max_rows, int64_t total_rows, int32_t n, int32_t k,
                    uint16_t *__restrict__ out, int32_t *__restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t *tile_a = smem;
-    uint8_t *tile_b = smem + kTileBytes;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 2 * kTileBytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + 2 * kTileBytes + 8);
-    volatile uint32_t *abort_flag = reinterpret_cast<uint32_t *>(smem + 2 * kTileBytes + 12);
+    const uint32_t a_ring = smem_addr(smem);
+    const uint32_t b_ring = a_ring + kStages * kTileBytes;
+    uint8_t *b_ring_ptr = smem + kStages * kTileBytes;
+    const uint32_t bars = a_ring + kBarrierOffset;  // full[kStages], empty[kStages], acc
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+    const uint32_t acc_bar = bars + 8u * (2 * kStages);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kBarrierOffset + 8 * (2 * kStages + 1));
+    volatile uint32_t *abort_flag = tmem_slot + 1;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -150,15 +195,17 @@ mx_moe_gemm_kernel(const uint16_t *__restrict__ a, const int64_t *__restrict__ e
         return;
     }
     if (m0 >= rows) return;  // this expert has fewer row tiles than the grid
-
-    const uint8_t *wp = w_packed + (int64_t)expert * n * (k / 2);
-    const uint8_t *ws = w_scales + (int64_t)expert * n * (k / 32);
-    const uint16_t *ap = a + row_begin * k;
+    const int nk = (k + kTileK - 1) / kTileK;
 
     if (tid == 0) {
-        mbar_init(smem_addr(bar), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), kDecodeThreads + 1);  // every decoder thread + the TMA arrival
+            mbar_init(empty_bar(s), 1);                  // the MMA commit
+        }
+        mbar_init(acc_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -172,90 +219,130 @@ mx_moe_gemm_kernel(const uint16_t *__restrict__ a, const int64_t *__restrict__ e
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const uint32_t a_base = smem_addr(tile_a);
-    const uint32_t b_base = smem_addr(tile_b);
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int k0 = 0; k0 < k && ok; k0 += kTileK) {
-        // activations: 128 rows x 8 chunks of 16 bytes
-#pragma unroll
-        for (int i = 0; i < (kTileM * 8) / kThreads; ++i) {
-            const uint32_t c = tid + i * kThreads;
-            const uint32_t r = c >> 3, kc = c & 7u;
-            const int64_t gm = m0 + r;
-            const int gk = k0 + (int)kc * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (gm < rows && gk < k) v = __ldg(reinterpret_cast<const uint4 *>(ap + gm * k + gk));
-            *reinterpret_cast<uint4 *>(tile_a + sw128_offset(r, kc)) = v;
-        }
-        // weights: 128 rows x 8 words of packed codes, decoded to 8 bf16 each
-#pragma unroll
-        for (int i = 0; i < (kTileN * 8) / kThreads; ++i) {
-            const uint32_t c = tid + i * kThreads;
-            const uint32_t r = c >> 3, kc = c & 7u;
-            const int gn = n0 + (int)r;
-            const int gk = k0 + (int)kc * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (gn < n && gk < k) {
-                const uint32_t w =
-                    __ldg(reinterpret_cast<const uint32_t *>(wp + (int64_t)gn * (k / 2) + gk / 2));
-                const uint32_t e = __ldg(ws + (int64_t)gn * (k / 32) + gk / 32);
-                v = mx_decode_word(w, mx_scaled_table(e));
+    if (warp < kDecodeWarps) {
+        // ---- decoder warps: weights (and, thread 0, the TMA of the activations) ----
+        const uint32_t r = (uint32_t)tid >> 1;  // weight row of the tile
+        const uint32_t h = (uint32_t)tid & 1u;  // which 32 codes of the 64-wide slice
+        const int gn = n0 + (int)r;
+        const uint8_t *wrow = w_packed + ((int64_t)expert * n + gn) * (k / 2);
+        const uint8_t *srow = w_scales + ((int64_t)expert * n + gn) * (k / 32);
+        auto load_raw = [&](int kt) {
+            RawSlice raw{make_uint4(0, 0, 0, 0), 127u};
+            const int kc = kt * kTileK + (int)h * 32;
+            if (kt < nk && gn < n && kc < k) {
+                raw.words = __ldg(reinterpret_cast<const uint4 *>(wrow + kc / 2));
+                raw.e8m0 = __ldg(srow + kc / 32);
             }
-            *reinterpret_cast<uint4 *>(tile_b + sw128_offset(r, kc)) = v;
+            return raw;
+        };
+        RawSlice cur = load_raw(0), nxt = load_raw(1);
+        for (int kt = 0; kt < nk; ++kt) {
+            const int s = kt % kStages;
+            const uint32_t use = (uint32_t)(kt / kStages);
+            const RawSlice ahead = load_raw(kt + 2);
+            if (kt >= kStages && !mbar_wait_bounded(empty_bar(s), (use - 1u) & 1u)) {
+                *abort_flag = 1;
+            }
+            if (*abort_flag) break;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(full_bar(s), kTileBytes);
+                tma_load_2d(a_ring + s * kTileBytes, &map_a, kt * kTileK, (int)(row_begin + m0),
+                            full_bar(s));
+            }
+            const ByteTable t = mx_scaled_table(cur.e8m0);
+            uint8_t *b_tile = b_ring_ptr + s * kTileBytes;
+            const uint32_t wv[4] = {cur.words.x, cur.words.y, cur.words.z, cur.words.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(b_tile + sw128_offset(r, h * 4 + j)) =
+                    mx_decode_word(wv[j], t);
+            // make these generic-proxy writes visible to the tensor core, then arrive
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(full_bar(s));
+            cur = nxt;
+            nxt = ahead;
         }
-        // make the generic-proxy shared-memory writes visible to the tensor core
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (tid == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
+        // ---- MMA issue: one thread ----
+        for (int kt = 0; kt < nk; ++kt) {
+            const int s = kt % kStages;
+            const uint32_t use = (uint32_t)(kt / kStages);
+            if (!mbar_wait_bounded(full_bar(s), use & 1u)) *abort_flag = 1;
+            if (*abort_flag) break;
             tc_fence_after();
+            const uint32_t a_s = a_ring + s * kTileBytes, b_s = b_ring + s * kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk)
-                mma_bf16(tmem, kmajor_sw128_desc(a_base + kk * 32),
-                         kmajor_sw128_desc(b_base + kk * 32), (k0 > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(smem_addr(bar));
+                mma_bf16(tmem, kmajor_sw128_desc(a_s + kk * 32), kmajor_sw128_desc(b_s + kk * 32),
+                         (kt > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
         }
-        // every thread waits until the tensor core has consumed the tiles
-        if (!mbar_wait_bounded(smem_addr(bar), phase)) *abort_flag = 1;
-        phase ^= 1u;
-        __syncthreads();
-        ok = (*abort_flag == 0);
+        mma_commit(acc_bar);  // fires when every MMA issued above has completed
     }
-    tc_fence_after();
 
-    if (ok) {
-        const int64_t row = m0 + warp * 32 + lane;
-        uint16_t *orow = out + (row_begin + row) * n;
+    // ---- epilogue: decoder warps read the accumulator ----
+    if (warp < kDecodeWarps) {
+        const bool done = mbar_wait_bounded(acc_bar, 0);
+        if (!done) *abort_flag = 1;
+        tc_fence_after();
+        if (done && *abort_flag == 0) {
+            const uint32_t quarter = (uint32_t)warp & 3u;  // TMEM lanes this warp may read
+            const int c_begin = (warp >> 2) * (kTileN / 2);
+            const int64_t row = m0 + quarter * 32 + lane;
+            uint16_t *orow = out + (row_begin + row) * n;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTileN; c0 += 32) {
-            uint32_t acc[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, acc);
-            if (row < rows && n0 + c0 < n) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c0);
+            for (int c0 = c_begin; c0 < c_begin + kTileN / 2; c0 += 32) {
+                uint32_t acc[32];
+                tmem_ld32(tmem + ((quarter * 32u) << 16) + (uint32_t)c0, acc);
+                if (row < rows && n0 + c0 < n) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c0);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 o;
-                    o.x = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 0]), __uint_as_float(acc[8 * q + 1]));
-                    o.y = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 2]), __uint_as_float(acc[8 * q + 3]));
-                    o.z = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 4]), __uint_as_float(acc[8 * q + 5]));
-                    o.w = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 6]), __uint_as_float(acc[8 * q + 7]));
-                    dst[q] = o;
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 o;
+                        o.x = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 0]), __uint_as_float(acc[8 * q + 1]));
+                        o.y = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 2]), __uint_as_float(acc[8 * q + 3]));
+                        o.z = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 4]), __uint_as_float(acc[8 * q + 5]));
+                        o.w = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 6]), __uint_as_float(acc[8 * q + 7]));
+                        dst[q] = o;
+                    }
                 }
             }
         }
-    } else if (tid == 0) {
-        atomicExch(status, FP4_ERR_TIMEOUT);
-        // give in-flight tensor-core work a last bounded chance to finish
-        mbar_wait_bounded(smem_addr(bar), phase);
     }
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {
+        if (tid == 0) {
+            atomicExch(status, FP4_ERR_TIMEOUT);
+            // give in-flight tensor-core work a last bounded chance to finish
+            mbar_wait_bounded(acc_bar, 0);
+        }
+        __syncthreads();
+    }
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
     }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled tensor_map_encoder() {
+    static EncodeTiled fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiled) nullptr;
+        return reinterpret_cast<EncodeTiled>(ptr);
+    }();
+    return fn;
 }
 
 }  // namespace
@@ -274,10 +361,23 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
         if (err != cudaSuccess) return err;
         configured_device = device;
     }
+    // TMA descriptor of the activations [total_rows, k] bf16: 64 x 128 boxes with the
+    // 128-byte swizzle; rows past total_rows and columns past k read as zero.
+    EncodeTiled encode = tensor_map_encoder();
+    if (encode == nullptr) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)(total_rows > 0 ? total_rows : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+    const cuuint32_t box[2] = {kTileK, kTileM};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a), dims, strides,
+               box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     const dim3 grid((unsigned)((n + kTileN - 1) / kTileN),
                     (unsigned)((max_rows + kTileM - 1) / kTileM), (unsigned)experts);
     mx_moe_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-        a, expert_offsets, w_packed, w_scales, max_rows, total_rows, (int32_t)n, (int32_t)k, out,
+        map, expert_offsets, w_packed, w_scales, max_rows, total_rows, (int32_t)n, (int32_t)k, out,
         status);
     return cudaGetLastError();
 }

@@ -173,7 +173,7 @@ fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_out, uint8_t
  *                        expert with more rows is not computed and status is set to
  *                        FP4_ERR_SHAPE)
  *   w_packed             device, uint8[experts * n * k / 2]: expert e's [n, k/2] codes
- *                        (as fp4_mx_unpack reads them); 4-byte aligned
+ *                        (as fp4_mx_unpack reads them); 16-byte aligned
  *   w_scales_e8m0        device, uint8[experts * n * k / 32]
  *   n, k                 output columns and reduction length, both multiples of 32
  *   total_rows           rows of a and out; an expert whose rows fall outside
