@@ -7,17 +7,21 @@
 // weights to bf16 and multiplies it with bf16 activations. Here the bf16 weights
 // never reach HBM: 0.53 bytes per weight are read instead of 2.
 //
-// One CTA owns a 128 x 128 output tile of one expert and runs a kStages-deep
-// shared-memory ring over 64-wide slices of K, with three roles:
-//   - the TMA engine loads each 128 x 64 bf16 activation tile (one thread issues
-//     cp.async.bulk.tensor with the 128-byte swizzle the tensor core reads);
+// One CTA owns a 128 x 128 output tile of one expert. The activation tiles and
+// the decoded weight tiles run in two separate shared-memory rings over 64-wide
+// slices of K, each with full/empty mbarriers:
+//   - one thread of the TMA warp keeps kStagesA activation tiles (128 x 64 bf16,
+//     cp.async.bulk.tensor with the 128-byte swizzle the tensor core reads) in
+//     flight ahead of the tensor core;
 //   - 8 decoder warps turn the expert's 128 x 64 MXFP4 weight tile into bf16 in
-//     the same swizzled K-major layout: each thread takes one row's 32 codes of
-//     the slice (one 16-byte load, one E8M0 byte, one scaled table), decoded in
-//     registers, with the raw words of the next two slices already in flight;
-//   - one thread of the MMA warp waits for a full stage, issues four
+//     the same swizzled K-major layout: each thread takes one row's 32 codes of a
+//     slice (one 16-byte load, one E8M0 byte, one scaled table), with the raw
+//     words of its next kAhead slices already in flight in registers; it decodes
+//     into registers before waiting for a free weight stage, so only the stores
+//     sit between the wait and the warp's single arrival;
+//   - one thread of the MMA warp waits for both tiles of a slice, issues four
 //     tcgen05.mma kind::f16 (M = 128, N = 128, K = 16) into the fp32 accumulator
-//     in tensor memory and commits the stage back to its "empty" barrier.
+//     in tensor memory and commits both stages back to their "empty" barriers.
 // The decoder warps then read the accumulator with tcgen05.ld, round to bf16
 // and store the tile.
 //
@@ -36,18 +40,21 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 constexpr int kTileK = 64;  // one 128-byte swizzle atom of bf16 along K
-constexpr int kStages = 3;
+constexpr int kStagesA = 4;      // activation tiles in flight (TMA)
+constexpr int kStagesB = 2;      // decoded weight tiles (the raw words run further ahead)
 constexpr int kDecodeWarps = 8;  // 2 threads per weight row: 256 threads
-constexpr int kMmaWarp = kDecodeWarps;
-constexpr int kThreads = (kDecodeWarps + 1) * 32;
-constexpr int kDecodeThreads = kDecodeWarps * 32;
+constexpr int kTmaWarp = kDecodeWarps;
+constexpr int kMmaWarp = kDecodeWarps + 1;
+constexpr int kThreads = (kDecodeWarps + 2) * 32;
+constexpr int kAhead = 5;        // raw weight slices in flight per decoder thread
+constexpr int kRing = kAhead + 1;
 constexpr uint32_t kTmemCols = 128;  // fp32 accumulator: one column per output column
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kTileBytes = kTileM * kTileK * 2;  // 16 KiB per operand tile and stage
 // shared memory: 1 KiB to align the tiles to the 1024-byte swizzle atom, the A
 // and B rings, then barriers, the tensor-memory address and the abort flag.
 // Two CTAs (2 x 128 tensor-memory columns) fit on an SM.
-constexpr int kBarrierOffset = 2 * kStages * kTileBytes;
+constexpr int kBarrierOffset = (kStagesA + kStagesB) * kTileBytes;
 constexpr int kSmemBytes = 1024 + kBarrierOffset + 256;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -132,6 +139,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Read-only global loads issued where they stand in the program (volatile asm
+// keeps them ahead of the work that follows), so that prefetched slices really
+// are in flight while earlier slices are decoded.
+__device__ __forceinline__ uint4 ldg_early_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_early_u8(const void *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// 16-byte store to a shared-memory address (always the shared-state space).
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // Byte offset of 16-byte chunk `kc` (8 bf16 along K) of row `r` in a tile of
 // 128-byte rows with the 128-byte swizzle (chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t kc) {
@@ -163,7 +193,7 @@ struct RawSlice {
     uint32_t e8m0;
 };
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const int64_t *__restrict__ expert_offsets,
                    const uint8_t *__restrict__ w_packed, const uint8_t *__restrict__ w_scales,
@@ -172,13 +202,16 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t a_ring = smem_addr(smem);
-    const uint32_t b_ring = a_ring + kStages * kTileBytes;
-    uint8_t *b_ring_ptr = smem + kStages * kTileBytes;
-    const uint32_t bars = a_ring + kBarrierOffset;  // full[kStages], empty[kStages], acc
-    auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
-    const uint32_t acc_bar = bars + 8u * (2 * kStages);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kBarrierOffset + 8 * (2 * kStages + 1));
+    const uint32_t b_ring = a_ring + kStagesA * kTileBytes;
+    // barriers: full/empty of each A stage, full/empty of each B stage, accumulator
+    const uint32_t bars = a_ring + kBarrierOffset;
+    auto full_a = [&](int s) { return bars + 8u * s; };
+    auto empty_a = [&](int s) { return bars + 8u * (kStagesA + s); };
+    auto full_b = [&](int s) { return bars + 8u * (2 * kStagesA + s); };
+    auto empty_b = [&](int s) { return bars + 8u * (2 * kStagesA + kStagesB + s); };
+    const uint32_t acc_bar = bars + 8u * (2 * kStagesA + 2 * kStagesB);
+    uint32_t *tmem_slot =
+        reinterpret_cast<uint32_t *>(smem + kBarrierOffset + 8 * (2 * kStagesA + 2 * kStagesB + 1));
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
     const int tid = threadIdx.x;
@@ -198,9 +231,13 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const int nk = (k + kTileK - 1) / kTileK;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), kDecodeThreads + 1);  // every decoder thread + the TMA arrival
-            mbar_init(empty_bar(s), 1);                  // the MMA commit
+        for (int s = 0; s < kStagesA; ++s) {
+            mbar_init(full_a(s), 1);   // the TMA thread's expect_tx arrival
+            mbar_init(empty_a(s), 1);  // the MMA commit
+        }
+        for (int s = 0; s < kStagesB; ++s) {
+            mbar_init(full_b(s), kDecodeWarps);  // one arrival per decoder warp
+            mbar_init(empty_b(s), 1);            // the MMA commit
         }
         mbar_init(acc_bar, 1);
         *abort_flag = 0;
@@ -220,78 +257,108 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kDecodeWarps) {
-        // ---- decoder warps: weights (and, thread 0, the TMA of the activations) ----
+        // ---- decoder warps: the expert's weights, one K slice after another ----
         const uint32_t r = (uint32_t)tid >> 1;  // weight row of the tile
         const uint32_t h = (uint32_t)tid & 1u;  // which 32 codes of the 64-wide slice
         const int gn = n0 + (int)r;
-        const uint8_t *wrow = w_packed + ((int64_t)expert * n + gn) * (k / 2);
-        const uint8_t *srow = w_scales + ((int64_t)expert * n + gn) * (k / 32);
+        const bool row_ok = gn < n;
+        const uint8_t *wrow = w_packed + ((int64_t)expert * n + (row_ok ? gn : 0)) * (k / 2) + h * 16;
+        const uint8_t *srow = w_scales + ((int64_t)expert * n + (row_ok ? gn : 0)) * (k / 32) + h;
         auto load_raw = [&](int kt) {
             RawSlice raw{make_uint4(0, 0, 0, 0), 127u};
-            const int kc = kt * kTileK + (int)h * 32;
-            if (kt < nk && gn < n && kc < k) {
-                raw.words = __ldg(reinterpret_cast<const uint4 *>(wrow + kc / 2));
-                raw.e8m0 = __ldg(srow + kc / 32);
+            if (kt < nk && row_ok && kt * kTileK + (int)h * 32 < k) {
+                raw.words = ldg_early_v4(wrow + kt * (kTileK / 2));
+                raw.e8m0 = ldg_early_u8(srow + kt * (kTileK / 32));
             }
             return raw;
         };
-        RawSlice cur = load_raw(0), nxt = load_raw(1);
-        for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt % kStages;
-            const uint32_t use = (uint32_t)(kt / kStages);
-            const RawSlice ahead = load_raw(kt + 2);
-            if (kt >= kStages && !mbar_wait_bounded(empty_bar(s), (use - 1u) & 1u)) {
-                *abort_flag = 1;
-            }
-            if (*abort_flag) break;
-            if (tid == 0) {
-                mbar_arrive_expect_tx(full_bar(s), kTileBytes);
-                tma_load_2d(a_ring + s * kTileBytes, &map_a, kt * kTileK, (int)(row_begin + m0),
-                            full_bar(s));
-            }
-            const ByteTable t = mx_scaled_table(cur.e8m0);
-            uint8_t *b_tile = b_ring_ptr + s * kTileBytes;
-            const uint32_t wv[4] = {cur.words.x, cur.words.y, cur.words.z, cur.words.w};
+        uint32_t st_off[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4 *>(b_tile + sw128_offset(r, h * 4 + j)) =
-                    mx_decode_word(wv[j], t);
-            // make these generic-proxy writes visible to the tensor core, then arrive
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(full_bar(s));
-            cur = nxt;
-            nxt = ahead;
+        for (int j = 0; j < 4; ++j) st_off[j] = sw128_offset(r, h * 4 + j);
+        RawSlice ring[kRing];
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i) ring[i] = load_raw(i);
+        bool stop = false;
+        for (int base = 0; base < nk && !stop; base += kRing) {
+#pragma unroll
+            for (int j = 0; j < kRing; ++j) {
+                const int kt = base + j;
+                if (kt >= nk) break;
+                const int s = kt % kStagesB;
+                const uint32_t use = (uint32_t)(kt / kStagesB);
+                ring[(j + kAhead) % kRing] = load_raw(kt + kAhead);
+                // decode into registers first: the arithmetic stays off the wait
+                const RawSlice cur = ring[j % kRing];
+                const ByteTable t = mx_scaled_table(cur.e8m0);
+                const uint4 d0 = mx_decode_word(cur.words.x, t);
+                const uint4 d1 = mx_decode_word(cur.words.y, t);
+                const uint4 d2 = mx_decode_word(cur.words.z, t);
+                const uint4 d3 = mx_decode_word(cur.words.w, t);
+                // one lane polls for the stage to be free; the warp follows via the vote
+                if (kt >= kStagesB && lane == 0 &&
+                    !mbar_wait_bounded(empty_b(s), (use - 1u) & 1u))
+                    *abort_flag = 1;
+                if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) {  // warp-uniform
+                    stop = true;
+                    break;
+                }
+                const uint32_t b_tile = b_ring + s * kTileBytes;
+                st_shared_v4(b_tile + st_off[0], d0);
+                st_shared_v4(b_tile + st_off[1], d1);
+                st_shared_v4(b_tile + st_off[2], d2);
+                st_shared_v4(b_tile + st_off[3], d3);
+                // make this thread's generic-proxy writes visible to the tensor core;
+                // after the warp has converged one lane arrives for all 32
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_b(s));
+            }
+        }
+    } else if (warp == kTmaWarp && lane == 0) {
+        // ---- TMA: activation tiles, kStagesA ahead of the tensor core ----
+        for (int kt = 0; kt < nk; ++kt) {
+            const int s = kt % kStagesA;
+            const uint32_t use = (uint32_t)(kt / kStagesA);
+            if (kt >= kStagesA && !mbar_wait_bounded(empty_a(s), (use - 1u) & 1u)) *abort_flag = 1;
+            if (*abort_flag) break;
+            mbar_arrive_expect_tx(full_a(s), kTileBytes);
+            tma_load_2d(a_ring + s * kTileBytes, &map_a, kt * kTileK, (int)(row_begin + m0),
+                        full_a(s));
         }
     } else if (warp == kMmaWarp && lane == 0) {
         // ---- MMA issue: one thread ----
         for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt % kStages;
-            const uint32_t use = (uint32_t)(kt / kStages);
-            if (!mbar_wait_bounded(full_bar(s), use & 1u)) *abort_flag = 1;
+            const int sa = kt % kStagesA, sb = kt % kStagesB;
+            if (!mbar_wait_bounded(full_a(sa), (uint32_t)(kt / kStagesA) & 1u) ||
+                !mbar_wait_bounded(full_b(sb), (uint32_t)(kt / kStagesB) & 1u))
+                *abort_flag = 1;
             if (*abort_flag) break;
             tc_fence_after();
-            const uint32_t a_s = a_ring + s * kTileBytes, b_s = b_ring + s * kTileBytes;
+            const uint32_t a_s = a_ring + sa * kTileBytes, b_s = b_ring + sb * kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk)
                 mma_bf16(tmem, kmajor_sw128_desc(a_s + kk * 32), kmajor_sw128_desc(b_s + kk * 32),
                          (kt > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+            // both stages are free once these MMAs have read them
+            mma_commit(empty_a(sa));
+            mma_commit(empty_b(sb));
         }
         mma_commit(acc_bar);  // fires when every MMA issued above has completed
     }
 
     // ---- epilogue: decoder warps read the accumulator ----
     if (warp < kDecodeWarps) {
-        const bool done = mbar_wait_bounded(acc_bar, 0);
-        if (!done) *abort_flag = 1;
+        if (lane == 0 && !mbar_wait_bounded(acc_bar, 0)) *abort_flag = 1;
+        const bool done = !__any_sync(0xFFFFFFFFu, *abort_flag != 0);  // warp-uniform
         tc_fence_after();
         if (done && *abort_flag == 0) {
             const uint32_t quarter = (uint32_t)warp & 3u;  // TMEM lanes this warp may read
-            const int c_begin = (warp >> 2) * (kTileN / 2);
+            constexpr int kCols = kTileN / (kDecodeWarps / 4);  // columns per warp (64)
+            const int c_begin = (warp >> 2) * kCols;
             const int64_t row = m0 + quarter * 32 + lane;
             uint16_t *orow = out + (row_begin + row) * n;
 #pragma unroll 1
-            for (int c0 = c_begin; c0 < c_begin + kTileN / 2; c0 += 32) {
+            for (int c0 = c_begin; c0 < c_begin + kCols; c0 += 32) {
                 uint32_t acc[32];
                 tmem_ld32(tmem + ((quarter * 32u) << 16) + (uint32_t)c0, acc);
                 if (row < rows && n0 + c0 < n) {
