@@ -34,6 +34,15 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
                                const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
                                int32_t *status, cudaStream_t stream);
 
+// The 128 x 256 all-TMA kernel the above dispatches to when eligible.
+bool mx_moe_gemm_wide_eligible(const uint8_t *w_packed, const uint8_t *w_scales, int64_t n,
+                               int64_t k);
+cudaError_t launch_mx_moe_gemm_wide(const uint16_t *a, const int64_t *expert_offsets,
+                                    int64_t experts, int64_t max_rows, int64_t total_rows,
+                                    const uint8_t *w_packed, const uint8_t *w_scales, int64_t n,
+                                    int64_t k, uint16_t *out, int32_t *status,
+                                    cudaStream_t stream);
+
 // Resident CTAs per SM x SM count for `kernel` at `threads` threads, cached per
 // device; a grid no larger than this runs in one wave.
 int max_resident_ctas(const void *kernel, int threads, int slot);

@@ -1,5 +1,7 @@
 // mx_moe_gemm.cu -- MoE expert GEMM with MXFP4 weights decoded into the tensor-core
-// B operand (tcgen05, sm_103a).
+// B operand (tcgen05, sm_103a): the general kernel (any k that is a multiple of
+// 32, 16-byte aligned weights, any scale alignment) and the dispatch; calls with
+// k <= 4096 and 16-byte aligned scales go to mx_moe_gemm_wide.cu.
 //
 // The consumer the pages' unpack serves: "vllm-project/vllm pull 51583",
 // "Motivation" and the comments on the unpack_B loop -- the CPU MoE GEMM
@@ -28,11 +30,11 @@
 // Every wait on an mbarrier is bounded: a wait that runs out records
 // FP4_ERR_TIMEOUT in the caller's status word and sets a shared abort flag; all
 // roles then stop issuing work, the tensor memory is freed and the CTA returns.
-#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
 
 #include "fp4_decode.cuh"
 #include "fp4mx.h"
 #include "launch.h"
+#include "tc_sm103.cuh"
 
 namespace fp4mx {
 namespace {
@@ -49,144 +51,12 @@ constexpr int kThreads = (kDecodeWarps + 2) * 32;
 constexpr int kAhead = 5;        // raw weight slices in flight per decoder thread
 constexpr int kRing = kAhead + 1;
 constexpr uint32_t kTmemCols = 128;  // fp32 accumulator: one column per output column
-constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kTileBytes = kTileM * kTileK * 2;  // 16 KiB per operand tile and stage
 // shared memory: 1 KiB to align the tiles to the 1024-byte swizzle atom, the A
 // and B rings, then barriers, the tensor-memory address and the abort flag.
 // Two CTAs (2 x 128 tensor-memory columns) fit on an SM.
 constexpr int kBarrierOffset = (kStagesA + kStagesB) * kTileBytes;
 constexpr int kSmemBytes = 1024 + kBarrierOffset + 256;
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// Shared-memory matrix descriptor of a K-major operand tile stored as rows of
-// 128 bytes with the 128-byte swizzle: start address / 16 in bits 0-13, the
-// stride between groups of 8 rows (1024 bytes) / 16 in bits 32-45, descriptor
-// version 1 in bits 46-47, swizzle mode 2 (128 B) in bits 61-63. The leading
-// byte offset is unused for this layout (one swizzle atom along K).
-__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
-           (2ull << 61);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
-// bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N / 8 in bits 17-22, M / 16 in bits 24-28.
-constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(phase)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for phase `phase` of the mbarrier; false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, phase)) return true;
-    return false;
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kInstrDesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
-}
-
-// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Read-only global loads issued where they stand in the program (volatile asm
-// keeps them ahead of the work that follows), so that prefetched slices really
-// are in flight while earlier slices are decoded.
-__device__ __forceinline__ uint4 ldg_early_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint32_t ldg_early_u8(const void *p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-// 16-byte store to a shared-memory address (always the shared-state space).
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-// Byte offset of 16-byte chunk `kc` (8 bf16 along K) of row `r` in a tile of
-// 128-byte rows with the 128-byte swizzle (chunk index XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t kc) {
-    return r * 128u + ((kc ^ (r & 7u)) << 4);
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-// TMA: 2-D tile (x = K offset in elements, y = row) of the tensor map into shared
-// memory, completing `bytes` of transaction count on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
 
 struct RawSlice {
     uint4 words;  // 32 packed codes of one weight row (4 words)
@@ -338,7 +208,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk)
                 mma_bf16(tmem, kmajor_sw128_desc(a_s + kk * 32), kmajor_sw128_desc(b_s + kk * 32),
-                         (kt > 0 || kk > 0) ? 1u : 0u);
+                         instr_desc_bf16<kTileM, kTileN>(), (kt > 0 || kk > 0) ? 1u : 0u);
             // both stages are free once these MMAs have read them
             mma_commit(empty_a(sa));
             mma_commit(empty_b(sb));
@@ -394,23 +264,6 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled tensor_map_encoder() {
-    static EncodeTiled fn = [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return (EncodeTiled) nullptr;
-        return reinterpret_cast<EncodeTiled>(ptr);
-    }();
-    return fn;
-}
 
 }  // namespace
 
@@ -418,6 +271,9 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
                                int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
                                const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
                                int32_t *status, cudaStream_t stream) {
+    if (mx_moe_gemm_wide_eligible(w_packed, w_scales, n, k))
+        return launch_mx_moe_gemm_wide(a, expert_offsets, experts, max_rows, total_rows, w_packed,
+                                       w_scales, n, k, out, status, stream);
     static thread_local int configured_device = -1;
     int device = 0;
     cudaError_t err = cudaGetDevice(&device);

@@ -16,7 +16,8 @@ def declared_functions():
     names = []
     for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
         if fn.endswith(".h"):
-            text = open(os.path.join(ROOT, "include", fn)).read()
+            with open(os.path.join(ROOT, "include", fn)) as fh:
+                text = fh.read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names += re.findall(r"\b(fp4_\w+)\s*\(", text)
     return sorted(set(names))

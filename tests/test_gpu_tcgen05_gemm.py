@@ -100,6 +100,38 @@ def test_moe_gate_up_shape(oracle_impl):
     run_case(oracle_impl, [128] * 32, 5760, 2880, seed=7)
 
 
+def test_general_kernel_large_k(oracle_impl):
+    """k above 4096 takes the general (128 x 128) kernel."""
+    run_case(oracle_impl, [40, 130], 160, 4096 + 64, seed=11)
+
+
+def test_general_kernel_unaligned_scales(oracle_impl):
+    """Scales that are not 16-byte aligned also take the general kernel; the result
+    must not depend on which kernel ran."""
+    rows, n, k = [96, 33], 320, 1024
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    rng = np.random.default_rng(12)
+    a_bits = inputs.bf16_normal_bits(rng, 129 * k).reshape(129, k)
+    w = inputs.mx_random(2 * n, k, 13, e_lo=118, e_hi=132)
+    packed = torch.from_numpy(w.packed.reshape(2, n, k // 2)).to(DEV)
+    scales_host = w.scales.reshape(2, n, k // 32)
+    buf = torch.zeros(scales_host.size + 16, dtype=torch.uint8, device=DEV)
+    buf[1:1 + scales_host.size] = torch.from_numpy(scales_host.reshape(-1)).to(DEV)
+    scales_odd = buf[1:1 + scales_host.size].view(2, n, k // 32)
+    scales_even = torch.from_numpy(scales_host).to(DEV)
+    a_t = torch.from_numpy(a_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    off_t = torch.from_numpy(offsets).to(DEV)
+    out_general, st1 = fp4.fp4_mx_moe_gemm(a_t, off_t, packed, scales_odd, 96)
+    out_wide, st2 = fp4.fp4_mx_moe_gemm(a_t, off_t, packed, scales_even, 96)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0 and int(st2.item()) == 0
+    exact, absdot = oracle_impl.mx_moe_gemm(a_bits, offsets, w.packed.reshape(2, n, k // 2),
+                                            scales_host)
+    for got in (out_general, out_wide):
+        g = got.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(g - exact) <= tolerance(exact, absdot, k))
+
+
 def test_rows_beyond_capacity_flagged(oracle_impl):
     """An expert with more rows than max_rows_per_expert is not computed and the
     status word says FP4_ERR_SHAPE."""
