@@ -10,10 +10,11 @@
 //     bytes, contiguous in memory) into shared memory, then streams the packed
 //     codes of the 256 x 64 weight slices (256 rows x 32 bytes, a 2-D uint8 tensor
 //     map) through a deep kStagesRaw ring;
-//   - 16 decoder warps read a slice's packed codes and scale bytes from shared
-//     memory (two threads per weight row, 32 codes each), release the raw stage,
-//     decode in registers and store the bf16 tile in the swizzled K-major layout
-//     of the tensor core's B operand (kStagesB ring);
+//   - 16 decoder warps in two groups that own alternating K slices read a
+//     slice's packed codes and scale
+//     bytes from shared memory (one thread per weight row: 64 codes, two E8M0
+//     blocks), release the raw stage, decode in registers and store the bf16 tile
+//     in the swizzled K-major layout of the tensor core's B operand;
 //   - one thread issues four tcgen05.mma kind::f16 (M = 128, N = 256, K = 16) per
 //     slice into a 256-column fp32 accumulator and commits the stages back.
 // A 256-wide tile halves the re-reads of the activations against 128-wide
@@ -33,10 +34,12 @@ namespace {
 constexpr int kM = 128;
 constexpr int kN = 256;
 constexpr int kK = 64;
-constexpr int kStagesA = 4;
-constexpr int kStagesRaw = 8;
-constexpr int kStagesB = 2;
-constexpr int kDecodeWarps = 16;  // 2 threads per weight row: 512 threads
+constexpr int kStagesA = 3;
+constexpr int kStagesRaw = 4;
+constexpr int kStagesB = 3;
+constexpr int kGroups = 2;        // decoder groups owning alternating K slices
+constexpr int kDecodeWarps = 16;  // two groups of 256 threads, one thread per weight row
+constexpr int kGroupWarps = kDecodeWarps / kGroups;
 constexpr int kTmaAWarp = kDecodeWarps;
 constexpr int kTmaWWarp = kDecodeWarps + 1;
 constexpr int kMmaWarp = kDecodeWarps + 2;
@@ -104,10 +107,10 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         for (int s = 0; s < kStagesRaw; ++s) {
             mbar_init(full_raw(s), 1);
-            mbar_init(empty_raw(s), kDecodeWarps);
+            mbar_init(empty_raw(s), kGroupWarps);  // the warps of the group owning the slice
         }
         for (int s = 0; s < kStagesB; ++s) {
-            mbar_init(full_b(s), kDecodeWarps);
+            mbar_init(full_b(s), kGroupWarps);  // one arrival per warp of the owning group
             mbar_init(empty_b(s), 1);
         }
         mbar_init(scale_bar, 1);
@@ -130,41 +133,48 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kDecodeWarps) {
-        // ---- decoder warps ----
-        const uint32_t r = (uint32_t)tid >> 1;  // weight row of the tile (0..255)
-        const uint32_t h = (uint32_t)tid & 1u;  // which 32 codes of the 64-wide slice
-        uint32_t st_off[4];
+        // ---- decoder warps: two groups of 8 warps own alternating K slices (group
+        // g takes kt = g, g + 2, ...); each thread decodes one whole row of its
+        // slices: 64 codes, two E8M0 blocks ----
+        const int group = warp / kGroupWarps;
+        const uint32_t r = (uint32_t)(tid - group * kGroupWarps * 32);  // 0..255
+        uint32_t st_off[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_off[j] = sw128_offset(r, h * 4 + j);
-        const uint32_t raw_off = r * 32u + h * 16u;
-        const uint32_t scale_row = scale_smem + r * (uint32_t)scale_pitch + h;
+        for (int j = 0; j < 8; ++j) st_off[j] = sw128_offset(r, (uint32_t)j);
+        const uint32_t raw_off = r * 32u;
+        const uint32_t scale_row = scale_smem + r * (uint32_t)scale_pitch;
         if (lane == 0 && !mbar_wait_bounded(scale_bar, 0)) *abort_flag = 1;
         bool stop = __any_sync(0xFFFFFFFFu, *abort_flag != 0);
-        for (int kt = 0; kt < nk && !stop; ++kt) {
+        for (int kt = group; kt < nk && !stop; kt += kGroups) {
             const int sr = kt % kStagesRaw, sb = kt % kStagesB;
+            const uint32_t use_b = (uint32_t)(kt / kStagesB);
+            const uint32_t b_tile = b_ring + sb * kBBytes;
             if (lane == 0 && !mbar_wait_bounded(full_raw(sr), (uint32_t)(kt / kStagesRaw) & 1u))
                 *abort_flag = 1;
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;  // warp-uniform
-            const uint4 words = lds_v4(raw_ring + sr * kRawBytes + raw_off);
-            const uint32_t e8m0 = (2 * kt + (int)h < scale_pitch)
-                                      ? lds_u8(scale_row + 2u * (uint32_t)kt)
-                                      : 127u;  // codes past k are zero-filled anyway
+            const uint4 w0 = lds_v4(raw_ring + sr * kRawBytes + raw_off);
+            const uint4 w1 = lds_v4(raw_ring + sr * kRawBytes + raw_off + 16u);
+            const uint32_t e0 = (2 * kt < scale_pitch) ? lds_u8(scale_row + 2u * (uint32_t)kt) : 127u;
+            const uint32_t e1 =
+                (2 * kt + 1 < scale_pitch) ? lds_u8(scale_row + 2u * (uint32_t)kt + 1u) : 127u;
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_raw(sr));  // the slice's raw bytes are in registers
-            const ByteTable t = mx_scaled_table(e8m0);
-            const uint4 d0 = mx_decode_word(words.x, t);
-            const uint4 d1 = mx_decode_word(words.y, t);
-            const uint4 d2 = mx_decode_word(words.z, t);
-            const uint4 d3 = mx_decode_word(words.w, t);
-            if (kt >= kStagesB && lane == 0 &&
-                !mbar_wait_bounded(empty_b(sb), (uint32_t)(kt / kStagesB - 1) & 1u))
+            const ByteTable t0 = mx_scaled_table(e0);
+            const ByteTable t1 = mx_scaled_table(e1);
+            uint4 d[8];
+            d[0] = mx_decode_word(w0.x, t0);
+            d[1] = mx_decode_word(w0.y, t0);
+            d[2] = mx_decode_word(w0.z, t0);
+            d[3] = mx_decode_word(w0.w, t0);
+            d[4] = mx_decode_word(w1.x, t1);
+            d[5] = mx_decode_word(w1.y, t1);
+            d[6] = mx_decode_word(w1.z, t1);
+            d[7] = mx_decode_word(w1.w, t1);
+            if (use_b > 0 && lane == 0 && !mbar_wait_bounded(empty_b(sb), (use_b - 1u) & 1u))
                 *abort_flag = 1;
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
-            const uint32_t b_tile = b_ring + sb * kBBytes;
-            st_shared_v4(b_tile + st_off[0], d0);
-            st_shared_v4(b_tile + st_off[1], d1);
-            st_shared_v4(b_tile + st_off[2], d2);
-            st_shared_v4(b_tile + st_off[3], d3);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) st_shared_v4(b_tile + st_off[j], d[j]);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(full_b(sb));
