@@ -49,7 +49,7 @@ UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("step", "mx_moe", "mx_stress", "mx_exhaustive", "nv_embedding_200k",
              "nv_embedding_32k", "nv_dequant_200k", "nv_dequant_32k", "mx_quantize_moe",
-             "mx_moe_gemm_128", "mx_moe_gemm_512")
+             "mx_moe_gemm_128", "mx_moe_gemm_512", "kv_pages")
 
 
 # ---------------------------------------------------------------------------
@@ -326,6 +326,48 @@ class NvDenseOp:
         return f"rows of the {self.x.name} table"
 
 
+class MxPagesOp:
+    """fp4_mx_unpack_pages of a page table against an MXFP4 KV pool."""
+    kind, kernel = "mx_unpack_pages", "mx_pages_rows_kernel"
+
+    def __init__(self, kv):
+        self.kv = kv
+        self.elems = kv.n_elems
+        self.bytes = kv.algorithmic_bytes()
+        self.min_bytes = self.bytes
+        self.units, self.elems_per_unit = kv.page_ids.size, kv.page_elems
+
+    def to_device(self, torch, dev):
+        self.ids = torch.from_numpy(self.kv.page_ids).to(dev)
+        self.p = torch.from_numpy(self.kv.pool.packed).to(dev)
+        self.s = torch.from_numpy(self.kv.pool.scales).to(dev)
+        self.o = torch.empty(*self.kv.page_ids.shape, self.kv.page_elems, dtype=torch.bfloat16,
+                             device=dev)
+
+    def launch(self, fp4, stream):
+        fp4.fp4_mx_unpack_pages(self.ids, self.p, self.s, out=self.o, stream=stream)
+
+    def e2e_jobs(self, torch, fp4, chunks):
+        hi = torch.from_numpy(self.kv.page_ids.reshape(-1)).pin_memory()
+        ids, o = self.ids.view(-1), self.o.view(-1, self.kv.page_elems)
+        ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+        jobs = []
+        for r0, r1 in _row_chunks(ids.shape[0], max(1, chunks // 2)):
+            def fn(st, r0=r0, r1=r1):
+                ids[r0:r1].copy_(hi[r0:r1], non_blocking=True)
+                fp4.fp4_mx_unpack_pages(ids[r0:r1], self.p, self.s, out=o[r0:r1], stream=st)
+                ho[r0:r1].copy_(o[r0:r1], non_blocking=True)
+            jobs.append(((r1 - r0) * 8, ho[r0:r1].numel() * 2, fn))
+        return jobs
+
+    def oracle_units(self, o, n, threads):
+        o.mx_unpack_pages(self.kv.page_ids.reshape(-1)[:n], self.kv.pool.packed,
+                          self.kv.pool.scales, threads)
+
+    def sample_name(self):
+        return "pages of the KV page table"
+
+
 class MxQuantOp:
     """fp4_mx_quantize of one bf16 [rows, k] tensor."""
     kind, kernel = "mx_quantize", "mx_quantize_words_kernel"
@@ -445,6 +487,7 @@ def load_workload(name: str):
         "nv_dequant_200k": lambda: [NvDenseOp(inputs.nv_embedding_200k())],
         "nv_dequant_32k": lambda: [NvDenseOp(inputs.nv_embedding_32k())],
         "mx_quantize_moe": lambda: [MxQuantOp(w) for w in inputs.bf16_moe()],
+        "kv_pages": lambda: [MxPagesOp(inputs.kv_pages())],
         "mx_moe_gemm_128": lambda: [MoeGemmOp(inputs.mx_moe()[0], 128)],
         "mx_moe_gemm_512": lambda: [MoeGemmOp(inputs.mx_moe()[0], 512)],
     }

@@ -12,6 +12,8 @@ status raise.
   applied as a wrapping int16 add of (E-127)<<7 into the bf16 exponent field,
   zero codes forced to +0.0 ("vllm-project/vllm pull 51583", "Motivation",
   "Implementation breakdown").
+* ``fp4_mx_unpack_pages(page_ids, packed_pool, scales_pool)`` -- the MXFP4 unpack
+  of pool pages picked by id (a paged FP4 KV cache with E8M0 scales).
 * ``fp4_mx_quantize(x_bf16)`` -- the inverse direction: bf16 -> (packed E2M1
   codes, E8M0 scales), by the OCP MX v1.0 conversion (the pages name the step,
   MXFP4QuantizeUtil.quantize, but not its rule).
@@ -28,7 +30,8 @@ from __future__ import annotations
 
 from ._lib import Status, last_error, library_path, load, status_string  # noqa: F401
 
-__all__ = ["fp4_mx_unpack", "fp4_mx_quantize", "fp4_mx_moe_gemm", "fp4_nv_embedding_gather",
+__all__ = ["fp4_mx_unpack", "fp4_mx_unpack_pages", "fp4_mx_quantize", "fp4_mx_moe_gemm",
+           "fp4_nv_embedding_gather",
            "fp4_nv_dequant",
            "fp4_status_string",
            "Fp4Error",
@@ -247,3 +250,37 @@ def fp4_mx_moe_gemm(a, expert_offsets, w_packed, w_scales, max_rows_per_expert: 
     if code != Status.OK:
         raise Fp4Error("fp4_mx_moe_gemm", code)
     return out, status
+
+
+def fp4_mx_unpack_pages(page_ids, packed_pool, scales_pool, out=None, err_flag=None,
+                        stream=None):
+    """Paged MXFP4 dequant: ``page_ids`` int64 (any shape), ``packed_pool`` uint8
+    [pool_pages, page_elems/2], ``scales_pool`` uint8 [pool_pages, page_elems/32] ->
+    bf16 [*page_ids.shape, page_elems], each row the fp4_mx_unpack of its page.
+    ``err_flag`` (optional int32 CUDA tensor) is set to Status.ERR_INDEX for ids
+    outside the pool; their rows are +0.0."""
+    torch = _torch()
+    _check_cuda(page_ids, "page_ids", (torch.int64,))
+    _check_cuda(packed_pool, "packed_pool", (torch.uint8,))
+    _check_cuda(scales_pool, "scales_pool", (torch.uint8,))
+    if packed_pool.dim() != 2 or scales_pool.dim() != 2:
+        raise ValueError("pools must be 2-D [pool_pages, ...]")
+    pool_pages, half = packed_pool.shape
+    page_elems = 2 * half
+    if page_elems % 32 or tuple(scales_pool.shape) != (pool_pages, page_elems // 32):
+        raise ValueError("scales_pool must be [pool_pages, page_elems/32], page_elems % 32 == 0")
+    shape = (*page_ids.shape, page_elems)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=packed_pool.device)
+    else:
+        _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
+        if tuple(out.shape) != shape:
+            raise ValueError(f"out must have shape {shape}")
+    if err_flag is not None:
+        _check_cuda(err_flag, "err_flag", (torch.int32,))
+    code = load().fp4_mx_unpack_pages(_ptr(page_ids), page_ids.numel(), _ptr(packed_pool),
+                                      _ptr(scales_pool), pool_pages, page_elems, _ptr(out),
+                                      _ptr(err_flag), _stream_handle(stream, packed_pool.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_mx_unpack_pages", code)
+    return out

@@ -40,6 +40,7 @@ SIGNATURES = {
                                 ctypes.c_int),
     "fp4_nv_dequant": ([_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp], ctypes.c_int),
     "fp4_mx_quantize": ([_vp, _vp, _vp, _i64, _i64, _vp], ctypes.c_int),
+    "fp4_mx_unpack_pages": ([_vp, _i64, _vp, _vp, _i64, _i64, _vp, _vp, _vp], ctypes.c_int),
     "fp4_mx_moe_gemm": ([_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp],
                         ctypes.c_int),
     "fp4_status_string": ([ctypes.c_int], ctypes.c_char_p),

@@ -232,6 +232,44 @@ FP4_EXPORT fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *exp
     return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_moe_gemm launch");
 }
 
+FP4_EXPORT fp4_status fp4_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,
+                                          const uint8_t *packed_pool,
+                                          const uint8_t *scales_pool_e8m0, int64_t pool_pages,
+                                          int64_t page_elems, uint16_t *out_bf16,
+                                          int32_t *err_flag, fp4_stream_t stream) {
+    clear_error();
+    if (num_pages < 0 || pool_pages < 0 || page_elems <= 0 || page_elems % 32 != 0)
+        return FP4_ERR_SHAPE;
+    if (num_pages == 0) return FP4_OK;
+    if (pool_pages == 0) return FP4_ERR_SHAPE;
+    if (num_pages > INT64_MAX / 2 / page_elems || pool_pages > INT64_MAX / page_elems)
+        return FP4_ERR_SHAPE;
+    if (page_ids == nullptr || packed_pool == nullptr || scales_pool_e8m0 == nullptr ||
+        out_bf16 == nullptr)
+        return FP4_ERR_NULL_PTR;
+    if (misaligned(page_ids, 8) || misaligned(out_bf16, 2) || misaligned(err_flag, 4))
+        return FP4_ERR_ALIGN;
+    const uint64_t out_bytes = (uint64_t)num_pages * (uint64_t)page_elems * 2;
+    const uint64_t pool_bytes = (uint64_t)pool_pages * (uint64_t)page_elems / 2;
+    if (overlaps(out_bf16, out_bytes, page_ids, (uint64_t)num_pages * 8) ||
+        overlaps(out_bf16, out_bytes, packed_pool, pool_bytes) ||
+        overlaps(out_bf16, out_bytes, scales_pool_e8m0, pool_bytes / 16) ||
+        (err_flag != nullptr &&
+         (overlaps(err_flag, 4, out_bf16, out_bytes) ||
+          overlaps(err_flag, 4, page_ids, (uint64_t)num_pages * 8) ||
+          overlaps(err_flag, 4, packed_pool, pool_bytes) ||
+          overlaps(err_flag, 4, scales_pool_e8m0, pool_bytes / 16))))
+        return FP4_ERR_ALIAS;
+    const void *ptrs[] = {page_ids, packed_pool, scales_pool_e8m0, out_bf16, err_flag};
+    const fp4_status s = check_pointers(ptrs, 5);
+    if (s != FP4_OK) return s;
+    const cudaError_t err =
+        fp4mx::launch_mx_unpack_pages(page_ids, num_pages, packed_pool, scales_pool_e8m0,
+                                      pool_pages, page_elems, out_bf16, err_flag,
+                                      (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_unpack_pages launch");
+}
+
 FP4_EXPORT fp4_status fp4_nv_dequant(const uint8_t *weight, const uint8_t *block_scale_e4m3,
                                      const float *global_scale, int64_t rows, int64_t hidden,
                                      int64_t group_size, uint16_t *out_bf16,
@@ -278,4 +316,4 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 103; }
+FP4_EXPORT int fp4_abi_version(void) { return 104; }

@@ -43,6 +43,13 @@ cudaError_t launch_mx_moe_gemm_wide(const uint16_t *a, const int64_t *expert_off
                                     int64_t k, uint16_t *out, int32_t *status,
                                     cudaStream_t stream);
 
+// Paged MXFP4 dequant: num_pages (> 0) pages of page_elems (a positive multiple of
+// 32) codes gathered from a pool by id.
+cudaError_t launch_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,
+                                   const uint8_t *packed, const uint8_t *scales,
+                                   int64_t pool_pages, int64_t page_elems, uint16_t *out,
+                                   int32_t *err_flag, cudaStream_t stream);
+
 // Resident CTAs per SM x SM count for `kernel` at `threads` threads, cached per
 // device; a grid no larger than this runs in one wave.
 int max_resident_ctas(const void *kernel, int threads, int slot);

@@ -29,6 +29,10 @@ mx_stress           2^30 packed bytes; each nibble a zero code with p = 0.3
                     codes; E per block uniform over {0, 107, 127, 137, 255}
 bf16_moe            (input of the quantiser) gate+up and down MoE weights as bf16,
                     standard normal / 10 as the pages' MoE test draws them
+kv_pages            (paged dequant) an MXFP4 KV pool of 32,768 pages of 16 tokens x
+                    8 heads x 128 dims (16,384 codes each), bytes uniform, E uniform
+                    in [118, 132]; a page table of 64 sequences x 128 pages drawn
+                    without replacement
 ==================  ==========================================================
 """
 from __future__ import annotations
@@ -312,3 +316,34 @@ def mx_stress(seed: int = 4) -> MxInput:
     packed = packed_with_zero_fraction(rng, rows * k // 2).reshape(rows, k // 2)
     scales = e8m0_choice(rng, rows * k // MX_BLOCK, (0, 107, 127, 137, 255))
     return MxInput(packed, scales.reshape(rows, k // MX_BLOCK), name="mx_stress")
+
+
+@dataclass
+class KvPagesInput:
+    page_ids: np.ndarray  # int64, any shape
+    pool: MxInput         # packed [pool_pages, page_elems/2], scales [pool_pages, page_elems/32]
+    name: str = ""
+
+    @property
+    def page_elems(self) -> int:
+        return self.pool.k
+
+    @property
+    def n_elems(self) -> int:
+        return self.page_ids.size * self.page_elems
+
+    def algorithmic_bytes(self) -> int:
+        """ids + the gathered pages' codes and scales + bf16 out."""
+        return self.page_ids.size * (8 + self.page_elems // 2 + self.page_elems // MX_BLOCK
+                                     + 2 * self.page_elems)
+
+
+def kv_pages(seed: int = 8, pool_pages: int = 32768, page_elems: int = 16 * 8 * 128,
+             table_shape=(64, 128)) -> KvPagesInput:
+    rng = np.random.default_rng(seed)
+    packed = uniform_bytes(rng, pool_pages * page_elems // 2).reshape(pool_pages, page_elems // 2)
+    scales = e8m0_uniform(rng, pool_pages * page_elems // MX_BLOCK, 118, 132)
+    pool = MxInput(packed, scales.reshape(pool_pages, page_elems // MX_BLOCK), name="kv_pool")
+    n = int(np.prod(table_shape))
+    ids = rng.permutation(pool_pages)[:n].astype(np.int64).reshape(table_shape)
+    return KvPagesInput(ids, pool, name=f"kv_pages_{pool_pages}x{page_elems}_table{n}")

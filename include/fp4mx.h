@@ -2,7 +2,7 @@
  * fp4mx.h -- C ABI of a GB300 (sm_103a) library that decodes block-scaled FP4
  * (E2M1) data into bf16.
  *
- * Five operations, each one CUDA kernel launch on the caller's stream:
+ * Six operations, each one CUDA kernel launch on the caller's stream:
  *
  *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
  *                             a wrapping 16-bit integer add into the bf16 exponent
@@ -12,6 +12,8 @@
  *                             value is multiplied by (block scale * global scale)
  *                             in fp32 and rounded to bf16 (nearest, ties to even).
  *   fp4_nv_dequant            the same NVFP4 decode over every row of a table.
+ *   fp4_mx_unpack_pages       the MXFP4 unpack of pages picked from a pool by id
+ *                             (a paged FP4 KV cache).
  *   fp4_mx_quantize           bf16 to MXFP4 (the inverse direction of the unpack).
  *   fp4_mx_moe_gemm           grouped MoE GEMM, MXFP4 weights decoded into the
  *                             tensor-core operand (tcgen05), bf16 activations.
@@ -126,6 +128,31 @@ fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_ids, const ui
                                    uint16_t *out_bf16, int32_t *err_flag, fp4_stream_t stream);
 
 /*
+ * fp4_mx_unpack_pages -- batched (paged) MXFP4 dequant, e.g. of an FP4 KV cache.
+ *
+ * "sgl-project/sglang pull 34222" (prhub digest), "Risks" item 3: the KV-cache
+ * path scales FP4 codes by E8M0 powers of two (batched_dequantize), unlike the
+ * NVFP4 embedding. A page table picks pages of an MXFP4 pool and each page is
+ * decoded by the fp4_mx_unpack rule:
+ *     out[i][:] = fp4_mx_unpack(pool page page_ids[i])
+ *
+ *   page_ids          device, int64[num_pages] (any logical shape, flattened)
+ *   num_pages         >= 0
+ *   packed_pool       device, uint8[pool_pages * page_elems / 2], [pool_pages, page_elems/2]
+ *   scales_pool_e8m0  device, uint8[pool_pages * page_elems / 32]
+ *   pool_pages        >= 1 when num_pages > 0
+ *   page_elems        codes per page, a positive multiple of 32 (else FP4_ERR_SHAPE)
+ *   out_bf16          device, uint16[num_pages * page_elems], row-major
+ *   err_flag          device int32 or NULL: a page id outside [0, pool_pages) gives a
+ *                     +0.0 row and sets *err_flag to FP4_ERR_INDEX (never cleared)
+ *   stream            CUDA stream the kernel is enqueued on
+ */
+fp4_status fp4_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,
+                               const uint8_t *packed_pool, const uint8_t *scales_pool_e8m0,
+                               int64_t pool_pages, int64_t page_elems, uint16_t *out_bf16,
+                               int32_t *err_flag, fp4_stream_t stream);
+
+/*
  * fp4_mx_quantize -- bf16 to MXFP4: E2M1 codes plus one E8M0 scale per 32.
  *
  * The inverse direction of fp4_mx_unpack. "vllm-project/vllm pull 51583"
@@ -222,7 +249,8 @@ const char *fp4_status_string(fp4_status status);
 const char *fp4_last_error(void);
 
 /* Version of this ABI (major * 100 + minor): 101 adds fp4_nv_dequant, 102 adds
- * fp4_mx_quantize and FP4_ERR_ALIGN, 103 adds fp4_mx_moe_gemm and FP4_ERR_TIMEOUT. */
+ * fp4_mx_quantize and FP4_ERR_ALIGN, 103 adds fp4_mx_moe_gemm and FP4_ERR_TIMEOUT,
+ * 104 adds fp4_mx_unpack_pages. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

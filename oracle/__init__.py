@@ -12,6 +12,9 @@ Functions and the passages they follow (web pages cited by title and section):
   "vllm-project/vllm pull 51583" (prhub digest), "Motivation" and
   "Implementation breakdown" items 1-2: E2M1 code -> bf16 bits, E8M0 scale as a
   wrapping int16 add of (E-127)<<7, zero codes forced to +0.0 lane by lane.
+* ``mx_unpack_pages`` -- batched (paged) MXFP4 dequant of a KV cache: the unpack
+  of the pool pages a page table names ("sgl-project/sglang pull 34222", "Risks"
+  item 3: the KV path's E8M0 power-of-two scales).
 * ``mx_quantize`` -- the step before the unpack (bf16 -> E2M1 codes + E8M0 per
   32), named but not printed by the same page; written from the OCP MX v1.0
   conversion (shared exponent floor(log2 amax) - 2, nearest-even rounding onto
@@ -116,6 +119,9 @@ def bind(path: str):
     lib.oracle_nv_dequant.restype = None
     lib.oracle_mx_quantize.argtypes = [_P16, ctypes.c_int64, _P8, _P8, ctypes.c_int]
     lib.oracle_mx_quantize.restype = None
+    lib.oracle_mx_unpack_pages.argtypes = [_P64, ctypes.c_int64, _P8, _P8, ctypes.c_int64,
+                                           ctypes.c_int64, _P16, ctypes.c_int]
+    lib.oracle_mx_unpack_pages.restype = ctypes.c_int64
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -188,6 +194,23 @@ class Oracle:
                                      _ptr(idx, ctypes.c_int64), idx.size,
                                      _ptr(out, ctypes.c_uint16))
         return out
+
+    def mx_unpack_pages(self, page_ids, packed_pool, scales_pool, threads: int = 1):
+        """Paged MXFP4 dequant: uint16[*page_ids.shape, page_elems] and the number of
+        page ids outside the pool (their rows are +0.0)."""
+        shape = np.shape(page_ids)
+        ids = _i64(page_ids).reshape(-1)
+        packed_pool, scales_pool = _u8(packed_pool), _u8(scales_pool)
+        pool_pages, half = packed_pool.shape
+        page_elems = 2 * half
+        if page_elems % 32 or scales_pool.shape != (pool_pages, page_elems // 32):
+            raise ValueError("pool must be [pages, page_elems/2] codes and [pages, page_elems/32] scales")
+        out = np.empty((ids.size, page_elems), dtype=np.uint16)
+        bad = self.lib.oracle_mx_unpack_pages(
+            _ptr(ids, ctypes.c_int64), ids.size, _ptr(packed_pool, ctypes.c_uint8),
+            _ptr(scales_pool, ctypes.c_uint8), pool_pages, page_elems,
+            _ptr(out, ctypes.c_uint16), int(threads))
+        return out.reshape(*shape, page_elems), int(bad)
 
     def mx_quantize(self, x_bf16_bits, threads: int = 1):
         """bf16 bit patterns (uint16[..., k], k % 32 == 0) -> (packed uint8[..., k/2],

@@ -346,6 +346,37 @@ void oracle_mx_quantize(const uint16_t *in_bf16, int64_t n_elems, uint8_t *packe
         mx_quantize_block(in_bf16 + b * 32, packed + b * 16, scales + b);
 }
 
+/* Batched (paged) MXFP4 dequant of a KV cache: out[i, :] = the MXFP4 unpack of
+ * pool page page_ids[i] ([pool_pages, page_elems/2] codes, [pool_pages,
+ * page_elems/32] E8M0). "sgl-project/sglang pull 34222", "Risks" item 3: the KV
+ * path scales FP4 by E8M0 powers of two (batched_dequantize), unlike the NVFP4
+ * embedding; the element rule taken is the MXFP4 unpack above. A page id outside
+ * [0, pool_pages) gives a +0.0 row; the return value counts them. */
+int64_t oracle_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages, const uint8_t *packed,
+                               const uint8_t *scales, int64_t pool_pages, int64_t page_elems,
+                               uint16_t *out, int threads) {
+    int64_t bad = 0;
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) reduction(+ : bad) num_threads(threads > 0 ? threads : 1)
+#endif
+    for (int64_t i = 0; i < num_pages; ++i) {
+        int64_t id = page_ids[i];
+        uint16_t *out_row = out + i * page_elems;
+        if (id < 0 || id >= pool_pages) {
+            for (int64_t j = 0; j < page_elems; ++j)
+                out_row[j] = 0;
+            bad += 1;
+            continue;
+        }
+        const uint8_t *page = packed + id * (page_elems / 2);
+        const uint8_t *page_scales = scales + id * (page_elems / 32);
+        for (int64_t j = 0; j < page_elems; ++j)
+            out_row[j] = mx_element(page, page_scales, j);
+    }
+    return bad;
+}
+
 /* Threads OpenMP would use (1 when built without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

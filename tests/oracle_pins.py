@@ -273,6 +273,23 @@ def pin_mx_element_order(o):
     assert np.all(out[2:32] == 0) and np.all(out[34:] == 0)
 
 
+def pin_mx_pages_are_unpacked_pool_pages(o):
+    """Each output row of the paged dequant is the MXFP4 unpack of the pool page its
+    id names (repeats allowed, id shape kept); ids outside the pool give +0.0 rows
+    and are counted."""
+    pool = inputs.mx_random(9, 256, seed=91, zero_fraction=True)
+    dense = o.mx_unpack(pool.packed, pool.scales).reshape(9, 256)
+    ids = np.array([[4, 0], [8, 4], [-1, 9]], dtype=np.int64)
+    out, bad = o.mx_unpack_pages(ids, pool.packed, pool.scales)
+    assert out.shape == (3, 2, 256) and bad == 2
+    flat = out.reshape(6, 256)
+    for i, pid in enumerate(ids.reshape(-1)):
+        if 0 <= pid < 9:
+            assert np.array_equal(flat[i], dense[pid])
+        else:
+            assert np.all(flat[i] == 0)
+
+
 def pin_mx_sampled_equals_full(o):
     x = inputs.mx_random(8, 256, seed=5)
     full = o.mx_unpack(x.packed, x.scales)

@@ -56,7 +56,7 @@ def test_status_strings(lib):
     for code in range(1, 11):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 103
+    assert lib.fp4_abi_version() == 104
 
 
 def test_mx_host_validation(lib):
@@ -141,6 +141,17 @@ def test_moe_gemm_host_validation(lib):
     base = ctypes.addressof(buf)
     base += (-base) % 16
     assert f(base + 8, base, 1, 8, base, base, 64, 64, 8, base, base, None) == fp4.Status.ERR_ALIGN
+
+
+def test_pages_host_validation(lib):
+    f = lib.fp4_mx_unpack_pages
+    g = lambda n, pool, elems: f(None, n, None, None, pool, elems, None, None, None)
+    assert g(2, 4, 48) == fp4.Status.ERR_SHAPE    # page_elems % 32
+    assert g(2, 4, 0) == fp4.Status.ERR_SHAPE
+    assert g(-1, 4, 64) == fp4.Status.ERR_SHAPE
+    assert g(0, 4, 64) == fp4.Status.OK
+    assert g(2, 0, 64) == fp4.Status.ERR_SHAPE    # ids but no pool
+    assert g(2, 4, 64) == fp4.Status.ERR_NULL_PTR
 
 
 def test_binding_refuses_cpu_tensors():

@@ -501,3 +501,62 @@ def test_mx_quantize_errors():
     assert lib.fp4_mx_quantize(x.data_ptr(), x.data_ptr() + 8, s.data_ptr(), 2, 64, None) == fp4.Status.ERR_ALIAS
     with pytest.raises(ValueError):
         fp4.fp4_mx_quantize(torch.zeros(2, 48, dtype=torch.bfloat16, device=DEV))
+
+
+# ---------------------------------------------------------------------------
+# paged MXFP4 dequant (KV cache)
+# ---------------------------------------------------------------------------
+
+def gpu_pages(ids, pool, err=None):
+    return fp4.fp4_mx_unpack_pages(torch.from_numpy(np.ascontiguousarray(ids)).to(DEV),
+                                   torch.from_numpy(pool.packed).to(DEV),
+                                   torch.from_numpy(pool.scales).to(DEV), err_flag=err)
+
+
+@pytest.mark.parametrize("pages,elems,ids_shape,seed", [(5, 32, (7,), 1), (9, 64, (3, 4), 2),
+                                                        (40, 2880, (33,), 3), (64, 16384, (2, 16), 4)])
+def test_mx_pages_shapes(ref, pages, elems, ids_shape, seed):
+    """Flat kernel (pages under 256 codes), segment kernel with ragged segments."""
+    pool = inputs.mx_random(pages, elems, seed, zero_fraction=True)
+    ids = np.random.default_rng(seed).integers(0, pages, size=ids_shape).astype(np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = gpu_pages(ids, pool, err)
+    want, bad = ref.mx_unpack_pages(ids, pool.packed, pool.scales)
+    assert tuple(got.shape) == want.shape and bad == 0 and int(err.item()) == 0
+    assert_same(bits(got), want, f"pages {pages}x{elems}")
+
+
+@pytest.mark.parametrize("elems", [64, 2880])
+def test_mx_pages_bad_ids(ref, elems):
+    pool = inputs.mx_random(6, elems, 7)
+    ids = np.array([2, -1, 6, 5, 2, 10 ** 12], dtype=np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = bits(gpu_pages(ids, pool, err))
+    want, bad = ref.mx_unpack_pages(ids, pool.packed, pool.scales)
+    assert bad == 3 and int(err.item()) == fp4.Status.ERR_INDEX
+    assert_same(got, want, "pages bad ids")
+
+
+def test_mx_pages_unaligned(ref):
+    pool = inputs.mx_random(11, 96, 8, zero_fraction=True)
+    ids = np.array([3, 0, 10, 3], dtype=np.int64)
+    pbuf = torch.zeros(pool.packed.size + 16, dtype=torch.uint8, device=DEV)
+    pbuf[1:1 + pool.packed.size] = torch.from_numpy(pool.packed.reshape(-1)).to(DEV)
+    obuf = torch.zeros(4 * 96 * 2 + 32, dtype=torch.uint8, device=DEV)
+    lib = fp4.load()
+    t_ids = torch.from_numpy(ids).to(DEV)
+    s = torch.from_numpy(pool.scales).to(DEV)
+    code = lib.fp4_mx_unpack_pages(t_ids.data_ptr(), 4, pbuf.data_ptr() + 1, s.data_ptr(), 11, 96,
+                                   obuf.data_ptr() + 2, None, torch.cuda.current_stream().cuda_stream)
+    assert code == 0
+    want, _ = ref.mx_unpack_pages(ids, pool.packed, pool.scales)
+    assert_same(obuf[2:2 + 4 * 96 * 2].cpu().numpy().view(np.uint16), want, "pages unaligned")
+
+
+def test_mx_pages_kv_workload(ref):
+    """The KV workload: 8,192 pages of 16,384 codes from a 32,768-page pool."""
+    kv = inputs.kv_pages()
+    got = bits(gpu_pages(kv.page_ids, kv.pool))
+    want, bad = ref.mx_unpack_pages(kv.page_ids, kv.pool.packed, kv.pool.scales, threads=THREADS)
+    assert bad == 0
+    assert_same(got, want, kv.name)

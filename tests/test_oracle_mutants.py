@@ -57,6 +57,11 @@ MUTATIONS = [
      "dense dequant scale row pitch wrong"),
     ("out[r * hidden + c] = nv_element(", "out[r * (hidden / 2) + c] = nv_element(",
      "dense dequant output row pitch wrong"),
+    ("const uint8_t *page_scales = scales + id * (page_elems / 32);",
+     "const uint8_t *page_scales = scales + i * (page_elems / 32);",
+     "paged dequant: scales of the wrong page"),
+    ("if (id < 0 || id >= pool_pages) {", "if (id < 0 || id > pool_pages) {",
+     "paged dequant: last valid page id off by one"),
     ("shared = (e - 1) - 2;", "shared = (e - 1) - 1;", "quantise: E2M1 emax taken as 1"),
     ("shared = (e - 1) - 2;", "shared = e - 2;", "quantise: floor(log2) off by one"),
     ("if (err < best_err || (err == best_err && (m % 2) == 0 && (best % 2) == 1)) {",
