@@ -20,6 +20,10 @@
 // A 256-wide tile halves the re-reads of the activations against 128-wide
 // tiles, and every global read is a bulk copy that the copy engine overlaps.
 //
+// When an expert can have more than 128 rows, each CTA owns two 128-row tiles of
+// the expert (two 256-column accumulators, all 512 tensor-memory columns) that
+// share every decoded weight tile, halving the decode work per FLOP.
+//
 // Used when k <= 4096 (the scale block fits in shared memory) and the weight and
 // scale buffers are 16-byte aligned; other calls take the general kernel.
 // Every mbarrier wait is bounded, as in the general kernel.
@@ -31,12 +35,10 @@
 namespace fp4mx {
 namespace {
 
-constexpr int kM = 128;
+constexpr int kM = 128;   // rows of one accumulator (one tensor-core M)
 constexpr int kN = 256;
 constexpr int kK = 64;
-constexpr int kStagesA = 3;
 constexpr int kStagesRaw = 4;
-constexpr int kStagesB = 3;
 constexpr int kGroups = 2;        // decoder groups owning alternating K slices
 constexpr int kDecodeWarps = 16;  // two groups of 256 threads, one thread per weight row
 constexpr int kGroupWarps = kDecodeWarps / kGroups;
@@ -44,20 +46,31 @@ constexpr int kTmaAWarp = kDecodeWarps;
 constexpr int kTmaWWarp = kDecodeWarps + 1;
 constexpr int kMmaWarp = kDecodeWarps + 2;
 constexpr int kThreads = (kDecodeWarps + 3) * 32;
-constexpr uint32_t kTmemCols = 256;
-constexpr int kABytes = kM * kK * 2;    // 16 KiB
-constexpr int kRawBytes = kN * kK / 2;  // 8 KiB
-constexpr int kBBytes = kN * kK * 2;    // 32 KiB
-constexpr int kScaleBytes = 32 * 1024;  // 256 rows x k/32 bytes: k <= 4096
-// shared-memory layout from a 1024-byte aligned base
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStagesA * kABytes;
-constexpr int kOffRaw = kOffB + kStagesB * kBBytes;
-constexpr int kOffScale = kOffRaw + kStagesRaw * kRawBytes;
-constexpr int kOffBar = kOffScale + kScaleBytes;
-constexpr int kSmemBytes = 1024 + kOffBar + 256;
-static_assert(kSmemBytes <= 232448, "shared memory per block");
+constexpr int kTileABytes = kM * kK * 2;  // 16 KiB: one 128 x 64 activation tile
+constexpr int kRawBytes = kN * kK / 2;    // 8 KiB
+constexpr int kBBytes = kN * kK * 2;      // 32 KiB
+constexpr int kScaleBytes = 32 * 1024;    // 256 rows x k/32 bytes: k <= 4096
 
+// kMT row tiles of 128 per CTA share every decoded weight tile: one accumulator
+// of 256 tensor-memory columns each (kMT = 2 fills the 512 columns).
+template <int kMT>
+struct WideCfg {
+    static constexpr int kRows = kM * kMT;
+    static constexpr int kStagesA = 3;
+    static constexpr int kStagesB = kMT == 1 ? 3 : 2;
+    static constexpr uint32_t kTmemCols = 256u * kMT;
+    static constexpr int kABytes = kMT * kTileABytes;
+    // shared-memory layout from a 1024-byte aligned base
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStagesA * kABytes;
+    static constexpr int kOffRaw = kOffB + kStagesB * kBBytes;
+    static constexpr int kOffScale = kOffRaw + kStagesRaw * kRawBytes;
+    static constexpr int kOffBar = kOffScale + kScaleBytes;
+    static constexpr int kSmemBytes = 1024 + kOffBar + 256;
+    static_assert(kSmemBytes <= 232448, "shared memory per block");
+};
+
+template <int kMT>
 __global__ void __launch_bounds__(kThreads, 1)
 mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_w,
@@ -65,6 +78,11 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
                         const uint8_t *__restrict__ w_scales, int64_t max_rows,
                         int64_t total_rows, int32_t n, int32_t k, uint16_t *__restrict__ out,
                         int32_t *__restrict__ status) {
+    using C = WideCfg<kMT>;
+    constexpr int kStagesA = C::kStagesA, kStagesB = C::kStagesB, kABytes = C::kABytes;
+    constexpr int kOffA = C::kOffA, kOffB = C::kOffB, kOffRaw = C::kOffRaw;
+    constexpr int kOffScale = C::kOffScale, kOffBar = C::kOffBar;
+    constexpr uint32_t kTmemCols = C::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = smem_addr(smem);
@@ -88,7 +106,7 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
     const int lane = tid & 31;
     const int expert = blockIdx.z;
     const int n0 = blockIdx.x * kN;
-    const int64_t m0 = (int64_t)blockIdx.y * kM;
+    const int64_t m0 = (int64_t)blockIdx.y * C::kRows;
     const int64_t row_begin = expert_offsets[expert];
     const int64_t rows = expert_offsets[expert + 1] - row_begin;
     // offsets live on the device: check them here, never read or write past the buffers
@@ -97,6 +115,8 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
         return;
     }
     if (m0 >= rows) return;  // this expert has fewer row tiles than the grid
+    // row tiles of this CTA that hold rows of the expert (the rest is neither loaded nor computed)
+    const int mt_live = (rows - m0 > (int64_t)kM) ? kMT : 1;
     const int nk = (k + kK - 1) / kK;
     const int scale_pitch = k / 32;
 
@@ -186,8 +206,12 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
             if (kt >= kStagesA && !mbar_wait_bounded(empty_a(s), (uint32_t)(kt / kStagesA - 1) & 1u))
                 *abort_flag = 1;
             if (*abort_flag) break;
-            mbar_arrive_expect_tx(full_a(s), kABytes);
-            tma_load_2d(a_ring + s * kABytes, &map_a, kt * kK, (int)(row_begin + m0), full_a(s));
+            mbar_arrive_expect_tx(full_a(s), (uint32_t)(mt_live * kTileABytes));
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt)
+                if (mt < mt_live)
+                        tma_load_2d(a_ring + s * kABytes + mt * kTileABytes, &map_a, kt * kK,
+                                (int)(row_begin + m0 + mt * kM), full_a(s));
         }
     } else if (warp == kTmaWWarp && lane == 0) {
         // ---- TMA: the tile's scales once, then the packed weight slices ----
@@ -218,9 +242,12 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
             tc_fence_after();
             const uint32_t a_s = a_ring + sa * kABytes, b_s = b_ring + sb * kBBytes;
 #pragma unroll
-            for (int kk = 0; kk < kK / 16; ++kk)
-                mma_bf16(tmem, kmajor_sw128_desc(a_s + kk * 32), kmajor_sw128_desc(b_s + kk * 32),
-                         idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+                for (int kk = 0; kk < kK / 16; ++kk)
+                    if (mt < mt_live)
+                        mma_bf16(tmem + mt * kN, kmajor_sw128_desc(a_s + mt * kTileABytes + kk * 32),
+                                 kmajor_sw128_desc(b_s + kk * 32), idesc, (kt > 0 || kk > 0) ? 1u : 0u);
             mma_commit(empty_a(sa));
             mma_commit(empty_b(sb));
         }
@@ -236,22 +263,25 @@ mx_moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a,
             const uint32_t quarter = (uint32_t)warp & 3u;  // TMEM lanes this warp may read
             constexpr int kCols = kN / (kDecodeWarps / 4);  // 64 columns per warp
             const int c_begin = (warp >> 2) * kCols;
-            const int64_t row = m0 + quarter * 32 + lane;
-            uint16_t *orow = out + (row_begin + row) * n;
 #pragma unroll 1
-            for (int c0 = c_begin; c0 < c_begin + kCols; c0 += 32) {
-                uint32_t acc[32];
-                tmem_ld32(tmem + ((quarter * 32u) << 16) + (uint32_t)c0, acc);
-                if (row < rows && n0 + c0 < n) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c0);
+            for (int mt = 0; mt < mt_live; ++mt) {
+                const int64_t row = m0 + mt * kM + quarter * 32 + lane;
+                uint16_t *orow = out + (row_begin + row) * n;
+#pragma unroll 1
+                for (int c0 = c_begin; c0 < c_begin + kCols; c0 += 32) {
+                    uint32_t acc[32];
+                    tmem_ld32(tmem + ((quarter * 32u) << 16) + (uint32_t)(mt * kN + c0), acc);
+                    if (row < rows && n0 + c0 < n) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c0);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 o;
-                        o.x = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 0]), __uint_as_float(acc[8 * q + 1]));
-                        o.y = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 2]), __uint_as_float(acc[8 * q + 3]));
-                        o.z = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 4]), __uint_as_float(acc[8 * q + 5]));
-                        o.w = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 6]), __uint_as_float(acc[8 * q + 7]));
-                        dst[q] = o;
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 o;
+                            o.x = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 0]), __uint_as_float(acc[8 * q + 1]));
+                            o.y = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 2]), __uint_as_float(acc[8 * q + 3]));
+                            o.z = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 4]), __uint_as_float(acc[8 * q + 5]));
+                            o.w = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 6]), __uint_as_float(acc[8 * q + 7]));
+                            dst[q] = o;
+                        }
                     }
                 }
             }
@@ -293,8 +323,13 @@ cudaError_t launch_mx_moe_gemm_wide(const uint16_t *a, const int64_t *expert_off
     cudaError_t err = cudaGetDevice(&device);
     if (err != cudaSuccess) return err;
     if (configured_device != device) {
-        err = cudaFuncSetAttribute(mx_moe_gemm_wide_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        err = cudaFuncSetAttribute(mx_moe_gemm_wide_kernel<1>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   WideCfg<1>::kSmemBytes);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(mx_moe_gemm_wide_kernel<2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       WideCfg<2>::kSmemBytes);
         if (err != cudaSuccess) return err;
         configured_device = device;
     }
@@ -306,7 +341,7 @@ cudaError_t launch_mx_moe_gemm_wide(const uint16_t *a, const int64_t *expert_off
     {
         const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)(total_rows > 0 ? total_rows : 1)};
         const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-        const cuuint32_t box[2] = {kK, kM};
+        const cuuint32_t box[2] = {kK, kM};  // one 128-row tile per TMA load
         if (encode(&map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a), dims,
                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -325,11 +360,22 @@ cudaError_t launch_mx_moe_gemm_wide(const uint16_t *a, const int64_t *expert_off
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const dim3 grid((unsigned)((n + kN - 1) / kN), (unsigned)((max_rows + kM - 1) / kM),
-                    (unsigned)experts);
-    mx_moe_gemm_wide_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-        map_a, map_w, expert_offsets, w_scales, max_rows, total_rows, (int32_t)n, (int32_t)k, out,
-        status);
+    // two 128-row tiles per CTA (sharing each decoded weight tile) once an expert
+    // can have more than 128 rows
+    if (max_rows > kM) {
+        const dim3 grid((unsigned)((n + kN - 1) / kN),
+                        (unsigned)((max_rows + WideCfg<2>::kRows - 1) / WideCfg<2>::kRows),
+                        (unsigned)experts);
+        mx_moe_gemm_wide_kernel<2><<<grid, kThreads, WideCfg<2>::kSmemBytes, stream>>>(
+            map_a, map_w, expert_offsets, w_scales, max_rows, total_rows, (int32_t)n, (int32_t)k,
+            out, status);
+    } else {
+        const dim3 grid((unsigned)((n + kN - 1) / kN), (unsigned)((max_rows + kM - 1) / kM),
+                        (unsigned)experts);
+        mx_moe_gemm_wide_kernel<1><<<grid, kThreads, WideCfg<1>::kSmemBytes, stream>>>(
+            map_a, map_w, expert_offsets, w_scales, max_rows, total_rows, (int32_t)n, (int32_t)k,
+            out, status);
+    }
     return cudaGetLastError();
 }
 

@@ -100,6 +100,26 @@ def test_moe_gate_up_shape(oracle_impl):
     run_case(oracle_impl, [128] * 32, 5760, 2880, seed=7)
 
 
+@pytest.mark.parametrize("rows,n,k", [([512, 300, 129, 0, 1], 512, 2880), ([256, 255, 257], 288, 704)])
+def test_two_row_tiles_per_cta(oracle_impl, rows, n, k):
+    """More than 128 rows per expert: each CTA owns two 128-row tiles sharing one
+    decoded weight tile; experts whose last tile pair holds one tile or a ragged
+    second tile included."""
+    run_case(oracle_impl, rows, n, k, seed=sum(rows) + k)
+
+
+def test_two_row_tiles_rows_beyond_capacity_flagged(oracle_impl):
+    """The capacity check holds for the two-tile kernel as well."""
+    k, n = 64, 64
+    offsets = torch.tensor([0, 10, 400], dtype=torch.int64, device=DEV)
+    a = torch.zeros(400, k, dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros(2, n, k // 2, dtype=torch.uint8, device=DEV)
+    s = torch.full((2, n, k // 32), 127, dtype=torch.uint8, device=DEV)
+    _, status = fp4.fp4_mx_moe_gemm(a, offsets, w, s, 256)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fp4.Status.ERR_SHAPE
+
+
 def test_general_kernel_large_k(oracle_impl):
     """k above 4096 takes the general (128 x 128) kernel."""
     run_case(oracle_impl, [40, 130], 160, 4096 + 64, seed=11)
