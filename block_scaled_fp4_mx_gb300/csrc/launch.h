@@ -28,20 +28,12 @@ cudaError_t launch_nv_dequant(const uint8_t *weight, const uint8_t *scales,
 cudaError_t launch_mx_quantize(const uint16_t *in, uint8_t *packed, uint8_t *scales,
                                int64_t n_elems, cudaStream_t stream);
 
-// Grouped MoE GEMM with MXFP4 weights decoded into the tensor-core B operand.
+// Grouped MoE GEMM with MXFP4 weights decoded into the tensor-core A operand in
+// tensor memory (any shape the entry point accepts; 16-byte aligned weights).
 cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets, int64_t experts,
                                int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
                                const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
                                int32_t *status, cudaStream_t stream);
-
-// The 128 x 256 all-TMA kernel the above dispatches to when eligible.
-bool mx_moe_gemm_wide_eligible(const uint8_t *w_packed, const uint8_t *w_scales, int64_t n,
-                               int64_t k);
-cudaError_t launch_mx_moe_gemm_wide(const uint16_t *a, const int64_t *expert_offsets,
-                                    int64_t experts, int64_t max_rows, int64_t total_rows,
-                                    const uint8_t *w_packed, const uint8_t *w_scales, int64_t n,
-                                    int64_t k, uint16_t *out, int32_t *status,
-                                    cudaStream_t stream);
 
 // Paged MXFP4 dequant: num_pages (> 0) pages of page_elems (a positive multiple of
 // 32) codes gathered from a pool by id.

@@ -1,36 +1,50 @@
-// mx_moe_gemm.cu -- MoE expert GEMM with MXFP4 weights decoded into the tensor-core
-// B operand (tcgen05, sm_103a): the general kernel (any k that is a multiple of
-// 32, 16-byte aligned weights, any scale alignment) and the dispatch; calls with
-// k <= 4096 and 16-byte aligned scales go to mx_moe_gemm_wide.cu.
+// mx_moe_gemm.cu -- grouped MoE GEMM with MXFP4 expert weights (sm_103a): a
+// persistent tcgen05 kernel whose decoded weight operand lives in tensor memory.
 //
 // The consumer the pages' unpack serves: "vllm-project/vllm pull 51583",
 // "Motivation" and the comments on the unpack_B loop -- the CPU MoE GEMM
 // (ops.fused_experts_cpu with CPUQuantMethod.MXFP4) unpacks a tile of MXFP4
 // weights to bf16 and multiplies it with bf16 activations. Here the bf16 weights
-// never reach HBM: 0.53 bytes per weight are read instead of 2.
+// never reach HBM (0.53 bytes per weight are read instead of 2 + 2 for unpack,
+// store and reload) and never touch shared memory either: bf16 activations x
+// MXFP4 weights decoded exactly as fp4_mx_unpack decodes them, fp32 accumulation
+// in tensor memory, bf16 out. The operands are swapped so that the decoded weights
+// can be the tensor core's A operand, which tcgen05.mma reads from tensor memory:
+//     D[weight row][token] = sum_k W[weight row][k] * X[token][k],
+// 128 weight rows per M tile (one per TMEM lane), the expert's tokens as N. A
+// decoder thread owns one weight row of a 64-wide K slice: it decodes the row's
+// 64 codes (two E8M0 blocks) in registers and writes them with one tcgen05.st
+// into its own TMEM lane, 32 columns of bf16 pairs. There is no shared-memory
+// copy of the decoded tile, no generic-to-async proxy fence, and the ring of
+// decoded slices can be deep because tensor memory is otherwise idle.
 //
-// One CTA owns a 128 x 128 output tile of one expert. The activation tiles and
-// the decoded weight tiles run in two separate shared-memory rings over 64-wide
-// slices of K, each with full/empty mbarriers:
-//   - one thread of the TMA warp keeps kStagesA activation tiles (128 x 64 bf16,
-//     cp.async.bulk.tensor with the 128-byte swizzle the tensor core reads) in
-//     flight ahead of the tensor core;
-//   - 8 decoder warps turn the expert's 128 x 64 MXFP4 weight tile into bf16 in
-//     the same swizzled K-major layout: each thread takes one row's 32 codes of a
-//     slice (one 16-byte load, one E8M0 byte, one scaled table), with the raw
-//     words of its next kAhead slices already in flight in registers; it decodes
-//     into registers before waiting for a free weight stage, so only the stores
-//     sit between the wait and the warp's single arrival;
-//   - one thread of the MMA warp waits for both tiles of a slice, issues four
-//     tcgen05.mma kind::f16 (M = 128, N = 128, K = 16) into the fp32 accumulator
-//     in tensor memory and commits both stages back to their "empty" barriers.
-// The decoder warps then read the accumulator with tcgen05.ld, round to bf16
-// and store the tile.
+// One CTA per SM walks a static list of work items (expert, token slab, tile of
+// weight rows; consecutive items share the expert's activation rows in L2). A
+// stage of the operand ring holds one 64-wide K slice: its activation tile in
+// shared memory and its decoded weights in tensor memory, under one "full"
+// barrier (the TMA bytes plus one arrival per decoder warp) and one "empty"
+// barrier (the MMA commit):
+//   - one TMA thread streams the activation tiles (kTok tokens x 64 bf16,
+//     128-byte swizzle, the MMA's B operand);
+//   - another streams the packed codes of the weight slices (rows x 32 bytes of
+//     a 2-D uint8 tensor map) through a ring of its own;
+//   - 16 decoder warps: warp w writes TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31,
+//     so 4 warps cover one 128-row M tile; the kMTw tiles of a slice take 4 kMTw
+//     warps and the remaining warps form further groups that own every kGroups-th
+//     slice; each thread loads its row's E8M0 bytes from global memory one slice
+//     ahead and takes the packed codes from shared memory;
+//   - one thread issues tcgen05.mma kind::f16 (M = 128, N = kTok, K = 16, A from
+//     TMEM), one asm block per slice that also probes the next stage's barrier
+//     ahead of the MMAs (tcgen05.mma issue blocks at the tensor rate, so every
+//     other instruction of this thread is tensor-pipe idle time);
+//   - an epilogue warpgroup reads finished accumulators with tcgen05.ld (a thread
+//     holds one weight row, i.e. one output column, for 32 tokens), rounds to
+//     bf16, pairs neighbouring columns with one lane exchange and stores 4-byte
+//     words: the 32 lanes of a warp write two 64-byte runs of two output rows.
 //
-// Every wait on an mbarrier is bounded: a wait that runs out records
-// FP4_ERR_TIMEOUT in the caller's status word and sets a shared abort flag; all
-// roles then stop issuing work, the tensor memory is freed and the CTA returns.
-
+// Every mbarrier wait is bounded: a wait that runs out sets an abort flag that
+// every role polls, and the launch reports FP4_ERR_TIMEOUT in the status word
+// after the MMA thread has drained its tensor-core work and TMEM is freed.
 #include "fp4_decode.cuh"
 #include "fp4mx.h"
 #include "launch.h"
@@ -39,80 +53,137 @@
 namespace fp4mx {
 namespace {
 
-constexpr int kTileM = 128;
-constexpr int kTileN = 128;
-constexpr int kTileK = 64;  // one 128-byte swizzle atom of bf16 along K
-constexpr int kStagesA = 4;      // activation tiles in flight (TMA)
-constexpr int kStagesB = 2;      // decoded weight tiles (the raw words run further ahead)
-constexpr int kDecodeWarps = 8;  // 2 threads per weight row: 256 threads
-constexpr int kTmaWarp = kDecodeWarps;
-constexpr int kMmaWarp = kDecodeWarps + 1;
-constexpr int kThreads = (kDecodeWarps + 2) * 32;
-constexpr int kAhead = 5;        // raw weight slices in flight per decoder thread
-constexpr int kRing = kAhead + 1;
-constexpr uint32_t kTmemCols = 128;  // fp32 accumulator: one column per output column
-constexpr int kTileBytes = kTileM * kTileK * 2;  // 16 KiB per operand tile and stage
-// shared memory: 1 KiB to align the tiles to the 1024-byte swizzle atom, the A
-// and B rings, then barriers, the tensor-memory address and the abort flag.
-// Two CTAs (2 x 128 tensor-memory columns) fit on an SM.
-constexpr int kBarrierOffset = (kStagesA + kStagesB) * kTileBytes;
-constexpr int kSmemBytes = 1024 + kBarrierOffset + 256;
+constexpr int kWM = 128;  // weight rows per M tile (TMEM lanes)
+constexpr int kK = 64;    // K per slice
+constexpr int kDecodeWarps = 16;
+constexpr int kEpiWarp0 = kDecodeWarps;
+constexpr int kEpiWarps = 4;
+constexpr int kTmaXWarp = kEpiWarp0 + kEpiWarps;
+constexpr int kTmaWWarp = kTmaXWarp + 1;
+constexpr int kMmaWarp = kTmaWWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kXBox = 128;                   // activation rows per TMA box
+constexpr int kXBoxBytes = kXBox * kK * 2;  // 16 KiB
 
-struct RawSlice {
-    uint4 words;  // 32 packed codes of one weight row (4 words)
-    uint32_t e8m0;
+template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_>
+struct TmemCfg {
+    static constexpr int kTok = kTok_;        // tokens per item (MMA N)
+    static constexpr int kMTw = kMTw_;        // 128-row weight tiles per item
+    static constexpr int kAccBufs = kAccBufs_;  // accumulator buffers
+    // a stage of the operand ring holds one slice's activation tile (shared memory)
+    // and its decoded weights (tensor memory) under one full and one empty barrier
+    static constexpr int S = kStages_, SR = kStagesRaw_;
+    static constexpr int kWRows = kWM * kMTw;
+    static constexpr int kWarpsPerSlice = 4 * kMTw;
+    static constexpr int kGroups = kDecodeWarps / kWarpsPerSlice;
+    // tensor memory: accumulator buffers, then the ring of decoded slices
+    static constexpr int kAccCols = kMTw * kTok;
+    static constexpr int kAColBase = kAccBufs * kAccCols;
+    static constexpr int kAStageCols = kMTw * (kK / 2);
+    // shared memory from a 1024-byte aligned base
+    static constexpr int kXBytes = kTok * kK * 2;
+    static constexpr int kRawBytes = kWRows * (kK / 2);
+    static constexpr int kOffX = 0;
+    static constexpr int kOffRaw = kOffX + S * kXBytes;
+    static constexpr int kOffBar = kOffRaw + SR * kRawBytes;
+    static constexpr int kNumBars = 2 * (S + SR) + 2 * kAccBufs + 1;
+    static constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
+    static_assert(kTok == 128 || kTok == 256, "MMA N");
+    static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
+    static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
+    static_assert(kAColBase + S * kAStageCols <= (int)kTmemCols, "tensor memory columns");
+    static_assert(kSmemBytes <= 232448, "shared memory per block");
 };
 
-__global__ void __launch_bounds__(kThreads, 2)
-mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const int64_t *__restrict__ expert_offsets,
-                   const uint8_t *__restrict__ w_packed, const uint8_t *__restrict__ w_scales,
-                   int64_t max_rows, int64_t total_rows, int32_t n, int32_t k,
-                   uint16_t *__restrict__ out, int32_t *__restrict__ status) {
+// Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
+using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
+// More tokens: 256 tokens per item against one weight tile.
+using CfgLarge = TmemCfg<256, 1, 1, 6, 8>;
+
+struct Item {
+    int64_t row_begin, rows, m0;
+    int expert, n0;
+    bool live, bad;
+};
+
+// Item t: weight tile t % n_tiles (fastest), token slab, expert.
+__device__ __forceinline__ Item item_at(int64_t t, int n_tiles, int slabs, int tok, int wrows,
+                                        const int64_t *__restrict__ offsets, int64_t max_rows,
+                                        int64_t total_rows) {
+    Item it;
+    const int64_t rest = t / n_tiles;
+    it.n0 = (int)(t - rest * n_tiles) * wrows;
+    it.expert = (int)(rest / slabs);
+    it.m0 = (rest - (int64_t)it.expert * slabs) * tok;
+    it.row_begin = __ldg(offsets + it.expert);
+    const int64_t end = __ldg(offsets + it.expert + 1);
+    it.rows = end - it.row_begin;
+    it.bad = it.row_begin < 0 || it.rows < 0 || it.rows > max_rows || end > total_rows;
+    it.live = !it.bad && it.m0 < it.rows;
+    return it;
+}
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1)
+mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
+                        const __grid_constant__ CUtensorMap map_w,
+                        const int64_t *__restrict__ expert_offsets,
+                        const uint8_t *__restrict__ w_scales, int32_t experts, int64_t max_rows,
+                        int64_t total_rows, int32_t n, int32_t k, uint16_t *__restrict__ out,
+                        int32_t *__restrict__ status) {
+    constexpr int kTok = C::kTok, kMTw = C::kMTw, S = C::S, SR = C::SR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    const uint32_t a_ring = smem_addr(smem);
-    const uint32_t b_ring = a_ring + kStagesA * kTileBytes;
-    // barriers: full/empty of each A stage, full/empty of each B stage, accumulator
-    const uint32_t bars = a_ring + kBarrierOffset;
-    auto full_a = [&](int s) { return bars + 8u * s; };
-    auto empty_a = [&](int s) { return bars + 8u * (kStagesA + s); };
-    auto full_b = [&](int s) { return bars + 8u * (2 * kStagesA + s); };
-    auto empty_b = [&](int s) { return bars + 8u * (2 * kStagesA + kStagesB + s); };
-    const uint32_t acc_bar = bars + 8u * (2 * kStagesA + 2 * kStagesB);
-    uint32_t *tmem_slot =
-        reinterpret_cast<uint32_t *>(smem + kBarrierOffset + 8 * (2 * kStagesA + 2 * kStagesB + 1));
+    const uint32_t base = smem_addr(smem);
+    const uint32_t x_ring = base + C::kOffX, raw_ring = base + C::kOffRaw;
+    const uint32_t bars = base + C::kOffBar;
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (S + s); };
+    auto full_raw = [&](int s) { return bars + 8u * (2 * S + s); };
+    auto empty_raw = [&](int s) { return bars + 8u * (2 * S + SR + s); };
+    auto acc_full = [&](int b) { return bars + 8u * (2 * (S + SR) + b); };
+    auto acc_empty = [&](int b) { return bars + 8u * (2 * (S + SR) + C::kAccBufs + b); };
+    const uint32_t drain_bar = bars + 8u * (C::kNumBars - 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kNumBars);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int expert = blockIdx.z;
-    const int n0 = blockIdx.x * kTileN;
-    const int64_t m0 = (int64_t)blockIdx.y * kTileM;
-    const int64_t row_begin = expert_offsets[expert];
-    const int64_t rows = expert_offsets[expert + 1] - row_begin;
-    // offsets live on the device: check them here, never read or write past the buffers
-    if (row_begin < 0 || rows < 0 || rows > max_rows || row_begin + rows > total_rows) {
-        if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicExch(status, FP4_ERR_SHAPE);
-        return;
-    }
-    if (m0 >= rows) return;  // this expert has fewer row tiles than the grid
-    const int nk = (k + kTileK - 1) / kTileK;
+    const int n_tiles = (n + C::kWRows - 1) / C::kWRows;
+    const int slabs = (int)((max_rows + kTok - 1) / kTok);
+    const int64_t n_items = (int64_t)experts * slabs * n_tiles;
+    const int nk = (k + kK - 1) / kK;
+    const int scale_pitch = k / 32;
+    auto item = [&](int64_t t) {
+        return item_at(t, n_tiles, slabs, kTok, C::kWRows, expert_offsets, max_rows, total_rows);
+    };
+    // tokens of an item that are computed: a slab whose live rows fit in 128 takes
+    // N = 128 MMAs and one activation box per slice
+    auto tok_live = [&](const Item &it) {
+        return (kTok == 256 && it.rows - it.m0 <= 128) ? 128 : kTok;
+    };
 
     if (tid == 0) {
-        for (int s = 0; s < kStagesA; ++s) {
-            mbar_init(full_a(s), 1);   // the TMA thread's expect_tx arrival
-            mbar_init(empty_a(s), 1);  // the MMA commit
+        for (int s = 0; s < S; ++s) {
+            // the activation TMA thread's arrival (with its bytes) and one per decoder warp
+            mbar_init(full(s), C::kWarpsPerSlice + 1);
+            mbar_init(empty(s), 1);
         }
-        for (int s = 0; s < kStagesB; ++s) {
-            mbar_init(full_b(s), kDecodeWarps);  // one arrival per decoder warp
-            mbar_init(empty_b(s), 1);            // the MMA commit
+        for (int s = 0; s < SR; ++s) {
+            mbar_init(full_raw(s), 1);
+            mbar_init(empty_raw(s), C::kWarpsPerSlice);
         }
-        mbar_init(acc_bar, 1);
+        for (int b = 0; b < C::kAccBufs; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -127,135 +198,229 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kDecodeWarps) {
-        // ---- decoder warps: the expert's weights, one K slice after another ----
-        const uint32_t r = (uint32_t)tid >> 1;  // weight row of the tile
-        const uint32_t h = (uint32_t)tid & 1u;  // which 32 codes of the 64-wide slice
-        const int gn = n0 + (int)r;
-        const bool row_ok = gn < n;
-        const uint8_t *wrow = w_packed + ((int64_t)expert * n + (row_ok ? gn : 0)) * (k / 2) + h * 16;
-        const uint8_t *srow = w_scales + ((int64_t)expert * n + (row_ok ? gn : 0)) * (k / 32) + h;
-        auto load_raw = [&](int kt) {
-            RawSlice raw{make_uint4(0, 0, 0, 0), 127u};
-            if (kt < nk && row_ok && kt * kTileK + (int)h * 32 < k) {
-                raw.words = ldg_early_v4(wrow + kt * (kTileK / 2));
-                raw.e8m0 = ldg_early_u8(srow + kt * (kTileK / 32));
-            }
-            return raw;
-        };
-        uint32_t st_off[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) st_off[j] = sw128_offset(r, h * 4 + j);
-        RawSlice ring[kRing];
-#pragma unroll
-        for (int i = 0; i < kAhead; ++i) ring[i] = load_raw(i);
+        // ---- decoders: slice g (counted across this CTA's items) belongs to group g % kGroups ----
+        const int quarter = warp & 3;
+        const int mt = (warp >> 2) % kMTw;
+        const int group = warp / C::kWarpsPerSlice;
+        const int r = mt * kWM + quarter * 32 + lane;  // weight row within the item
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)C::kAColBase +
+                                   (uint32_t)(mt * (kK / 2));
         bool stop = false;
-        for (int base = 0; base < nk && !stop; base += kRing) {
-#pragma unroll
-            for (int j = 0; j < kRing; ++j) {
-                const int kt = base + j;
-                if (kt >= nk) break;
-                const int s = kt % kStagesB;
-                const uint32_t use = (uint32_t)(kt / kStagesB);
-                ring[(j + kAhead) % kRing] = load_raw(kt + kAhead);
-                // decode into registers first: the arithmetic stays off the wait
-                const RawSlice cur = ring[j % kRing];
-                const ByteTable t = mx_scaled_table(cur.e8m0);
-                const uint4 d0 = mx_decode_word(cur.words.x, t);
-                const uint4 d1 = mx_decode_word(cur.words.y, t);
-                const uint4 d2 = mx_decode_word(cur.words.z, t);
-                const uint4 d3 = mx_decode_word(cur.words.w, t);
-                // one lane polls for the stage to be free; the warp follows via the vote
-                if (kt >= kStagesB && lane == 0 &&
-                    !mbar_wait_bounded(empty_b(s), (use - 1u) & 1u))
-                    *abort_flag = 1;
+        uint32_t g0 = 0;  // first slice of the current item
+        // ring positions of this group's next slice g (the group's slices are g =
+        // group, group + kGroups, ... across items): stage and phase of each ring
+        int sr = group % SR, sw = group % S;
+        uint32_t pr = (uint32_t)(group / SR) & 1u, pw = (uint32_t)(group / S) & 1u;
+        uint32_t g = (uint32_t)group;
+        for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
+            const Item it = item(t);
+            if (!it.live) continue;
+            const bool row_ok = it.n0 + r < n;
+            const uint8_t *srow = w_scales + ((int64_t)it.expert * n + it.n0 + r) * scale_pitch;
+            // the row's two E8M0 bytes of slice kt; those of the group's next slice
+            // are loaded one slice ahead, so their latency hides behind a slice
+            auto scale_at = [&](int kt, int h) {
+                return (row_ok && 2 * kt + h < scale_pitch) ? ldg_early_u8(srow + 2 * kt + h) : 127u;
+            };
+            const int kt_first = (int)(((uint32_t)group + (uint32_t)C::kGroups -
+                                        g0 % (uint32_t)C::kGroups) % (uint32_t)C::kGroups);
+            uint32_t next_e0 = scale_at(kt_first, 0), next_e1 = scale_at(kt_first, 1);
+            for (int kt = kt_first; kt < nk; kt += C::kGroups) {
+                const uint32_t e0 = next_e0, e1 = next_e1;
+                if (kt + C::kGroups < nk) {
+                    next_e0 = scale_at(kt + C::kGroups, 0);
+                    next_e1 = scale_at(kt + C::kGroups, 1);
+                }
+                if (lane == 0 && !mbar_wait_bounded(full_raw(sr), pr)) *abort_flag = 1;
                 if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) {  // warp-uniform
                     stop = true;
                     break;
                 }
-                const uint32_t b_tile = b_ring + s * kTileBytes;
-                st_shared_v4(b_tile + st_off[0], d0);
-                st_shared_v4(b_tile + st_off[1], d1);
-                st_shared_v4(b_tile + st_off[2], d2);
-                st_shared_v4(b_tile + st_off[3], d3);
-                // make this thread's generic-proxy writes visible to the tensor core;
-                // after the warp has converged one lane arrives for all 32
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const uint32_t raw_row = raw_ring + sr * C::kRawBytes + (uint32_t)r * 32u;
+                const uint4 w0 = lds_v4(raw_row);
+                const uint4 w1 = lds_v4(raw_row + 16u);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_b(s));
+                if (lane == 0) mbar_arrive(empty_raw(sr));  // the slice's codes are in registers
+                const ByteTable t0 = mx_scaled_table(e0);
+                const ByteTable t1 = mx_scaled_table(e1);
+                uint32_t d[32];
+                const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = mx_decode_word(words[q], q < 4 ? t0 : t1);
+                    d[4 * q + 0] = v.x;
+                    d[4 * q + 1] = v.y;
+                    d[4 * q + 2] = v.z;
+                    d[4 * q + 3] = v.w;
+                }
+                if (g >= (uint32_t)S && lane == 0 && !mbar_wait_bounded(empty(sw), pw ^ 1u))
+                    *abort_flag = 1;
+                if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st32(lane_addr + (uint32_t)(sw * C::kAStageCols), d);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full(sw));
+                g += C::kGroups;
+                if ((sr += C::kGroups) >= SR) { sr -= SR; pr ^= 1u; }
+                if ((sw += C::kGroups) >= S) { sw -= S; pw ^= 1u; }
             }
+            g0 += (uint32_t)nk;
         }
-    } else if (warp == kTmaWarp && lane == 0) {
-        // ---- TMA: activation tiles, kStagesA ahead of the tensor core ----
-        for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt % kStagesA;
-            const uint32_t use = (uint32_t)(kt / kStagesA);
-            if (kt >= kStagesA && !mbar_wait_bounded(empty_a(s), (use - 1u) & 1u)) *abort_flag = 1;
-            if (*abort_flag) break;
-            mbar_arrive_expect_tx(full_a(s), kTileBytes);
-            tma_load_2d(a_ring + s * kTileBytes, &map_a, kt * kTileK, (int)(row_begin + m0),
-                        full_a(s));
-        }
-    } else if (warp == kMmaWarp && lane == 0) {
-        // ---- MMA issue: one thread ----
-        for (int kt = 0; kt < nk; ++kt) {
-            const int sa = kt % kStagesA, sb = kt % kStagesB;
-            if (!mbar_wait_bounded(full_a(sa), (uint32_t)(kt / kStagesA) & 1u) ||
-                !mbar_wait_bounded(full_b(sb), (uint32_t)(kt / kStagesB) & 1u))
-                *abort_flag = 1;
-            if (*abort_flag) break;
+    } else if (warp < kEpiWarp0 + kEpiWarps) {
+        // ---- epilogue: accumulator (weight rows x tokens) -> bf16 output ----
+        const int quarter = warp & 3;
+        uint32_t use[2] = {0, 0};
+        uint32_t j = 0;  // live items so far
+        bool stop = false;
+        for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
+            const Item it = item(t);
+            if (!it.live) continue;
+            const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
+            const uint32_t u = b ? use[1] : use[0];
+            if (lane == 0 && !mbar_wait_bounded(acc_full(b), u & 1u)) *abort_flag = 1;
+            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             tc_fence_after();
-            const uint32_t a_s = a_ring + sa * kTileBytes, b_s = b_ring + sb * kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < kTileK / 16; ++kk)
-                mma_bf16(tmem, kmajor_sw128_desc(a_s + kk * 32), kmajor_sw128_desc(b_s + kk * 32),
-                         instr_desc_bf16<kTileM, kTileN>(), (kt > 0 || kk > 0) ? 1u : 0u);
-            // both stages are free once these MMAs have read them
-            mma_commit(empty_a(sa));
-            mma_commit(empty_b(sb));
-        }
-        mma_commit(acc_bar);  // fires when every MMA issued above has completed
-    }
-
-    // ---- epilogue: decoder warps read the accumulator ----
-    if (warp < kDecodeWarps) {
-        if (lane == 0 && !mbar_wait_bounded(acc_bar, 0)) *abort_flag = 1;
-        const bool done = !__any_sync(0xFFFFFFFFu, *abort_flag != 0);  // warp-uniform
-        tc_fence_after();
-        if (done && *abort_flag == 0) {
-            const uint32_t quarter = (uint32_t)warp & 3u;  // TMEM lanes this warp may read
-            constexpr int kCols = kTileN / (kDecodeWarps / 4);  // columns per warp (64)
-            const int c_begin = (warp >> 2) * kCols;
-            const int64_t row = m0 + quarter * 32 + lane;
-            uint16_t *orow = out + (row_begin + row) * n;
+            const int64_t tok_rows = it.rows - it.m0;  // > 0
+            const int n_tok = (int)(tok_rows < kTok ? tok_rows : kTok);
+            const int c_end = (n_tok + 31) & ~31;
+            const bool odd = lane & 1;
 #pragma unroll 1
-            for (int c0 = c_begin; c0 < c_begin + kCols; c0 += 32) {
-                uint32_t acc[32];
-                tmem_ld32(tmem + ((quarter * 32u) << 16) + (uint32_t)c0, acc);
-                if (row < rows && n0 + c0 < n) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c0);
+            for (int mt = 0; mt < kMTw; ++mt) {
+                // lanes 2i and 2i+1 hold output columns c and c+1 (c even); after an
+                // exchange the even lane stores both columns of token t and the odd
+                // lane both columns of token t + 1
+                const int col = it.n0 + mt * kWM + quarter * 32 + (lane & ~1);
+                const bool col_ok = col < n;
+                uint16_t *optr = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n + col;
+                const int64_t step2 = 2 * (int64_t)n;
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
+                                       (uint32_t)(b * C::kAccCols + mt * kTok);
+#pragma unroll 1
+                for (int c0 = 0; c0 < c_end; c0 += 32) {
+                    uint32_t acc[32];
+                    tmem_ld32(taddr + (uint32_t)c0, acc);
+                    if (mt == kMTw - 1 && c0 + 32 >= c_end) {  // the buffer is read out
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty(b));
+                    }
+                    const int lim = n_tok - c0 - (odd ? 1 : 0);  // tokens q (even) with q < lim are stored
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 o;
-                        o.x = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 0]), __uint_as_float(acc[8 * q + 1]));
-                        o.y = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 2]), __uint_as_float(acc[8 * q + 3]));
-                        o.z = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 4]), __uint_as_float(acc[8 * q + 5]));
-                        o.w = pack_bf16x2_rn(__uint_as_float(acc[8 * q + 6]), __uint_as_float(acc[8 * q + 7]));
-                        dst[q] = o;
+                    for (int q = 0; q < 32; q += 2) {
+                        const uint32_t mine =
+                            pack_bf16x2_rn(__uint_as_float(acc[q]), __uint_as_float(acc[q + 1]));
+                        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+                        const uint32_t word = odd ? prmt(other, mine, 0x7632u) : prmt(mine, other, 0x5410u);
+                        if (col_ok && q < lim) *reinterpret_cast<uint32_t *>(optr) = word;
+                        optr += step2;
                     }
                 }
             }
+            if (b) ++use[1]; else ++use[0];
+            ++j;
         }
+    } else if (warp == kTmaXWarp && lane == 0) {
+        // ---- TMA: activation tiles ----
+        int s = 0;
+        uint32_t ph = 0, g = 0;
+        bool stop = false;
+        for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
+            const Item it = item(t);
+            if (!it.live) continue;
+            const int boxes = tok_live(it) / kXBox;
+            const int row0 = (int)(it.row_begin + it.m0);
+            for (int kt = 0; kt < nk; ++kt, ++g) {
+                if (g >= (uint32_t)S && !mbar_wait_bounded(empty(s), ph ^ 1u)) *abort_flag = 1;
+                if (*abort_flag) {
+                    stop = true;
+                    break;
+                }
+                mbar_arrive_expect_tx(full(s), (uint32_t)(boxes * kXBoxBytes));
+                for (int bx = 0; bx < boxes; ++bx)
+                    tma_load_2d(x_ring + s * C::kXBytes + bx * kXBoxBytes, &map_x, kt * kK,
+                                row0 + bx * kXBox, full(s));
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+        }
+    } else if (warp == kTmaWWarp && lane == 0) {
+        // ---- TMA: packed weight slices ----
+        int s = 0;
+        uint32_t ph = 0, g = 0;
+        bool stop = false;
+        for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
+            const Item it = item(t);
+            if (!it.live) continue;
+            const int w_row = it.expert * n + it.n0;
+            for (int kt = 0; kt < nk; ++kt, ++g) {
+                if (g >= (uint32_t)SR && !mbar_wait_bounded(empty_raw(s), ph ^ 1u)) *abort_flag = 1;
+                if (*abort_flag) {
+                    stop = true;
+                    break;
+                }
+                mbar_arrive_expect_tx(full_raw(s), (uint32_t)C::kRawBytes);
+                tma_load_2d(raw_ring + s * C::kRawBytes, &map_w, kt * (kK / 2), w_row, full_raw(s));
+                if (++s == SR) { s = 0; ph ^= 1u; }
+            }
+        }
+    } else if (warp == kMmaWarp && lane == 0) {
+        // ---- MMA issue ----
+        constexpr uint32_t idesc_full = instr_desc_bf16<kWM, kTok>();
+        constexpr uint32_t idesc_half = instr_desc_bf16<kWM, 128>();
+        // stage 0 descriptors; stage s and K step kk add s * bytes/16 and kk * 32/16
+        const uint64_t x_desc0 = kmajor_sw128_desc(x_ring);
+        const uint32_t a_col0 = tmem + (uint32_t)C::kAColBase;
+        uint32_t use[2] = {0, 0};
+        uint32_t j = 0;
+        int st = 0;
+        uint32_t ph = 0;
+        uint32_t ready = 0;  // the next stage's full barrier was seen complete
+        bool stop = false;
+        for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
+            const Item it = item(t);
+            if (it.bad) atomicExch(status, FP4_ERR_SHAPE);
+            if (!it.live) continue;
+            const uint32_t idesc = tok_live(it) == kTok ? idesc_full : idesc_half;
+            const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
+            const uint32_t u = b ? use[1] : use[0];
+            // the buffer's previous item must have been read out
+            if (u > 0 && !mbar_wait_bounded(acc_empty(b), (u - 1u) & 1u)) *abort_flag = 1;
+            const uint32_t d_col = tmem + (uint32_t)(b * C::kAccCols);
+            for (int kt = 0; kt < nk; ++kt) {
+                if (!ready && !mbar_wait_bounded(full(st), ph)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const int st_next = st + 1 == S ? 0 : st + 1;
+                const uint32_t ph_next = st + 1 == S ? ph ^ 1u : ph;
+                ready = mma_slice_tmem_a<kMTw, kTok>(
+                    d_col, a_col0 + (uint32_t)(st * C::kAStageCols),
+                    x_desc0 + (uint64_t)(st * (C::kXBytes >> 4)), idesc, kt > 0 ? 1u : 0u,
+                    empty(st), full(st_next), ph_next);
+                st = st_next;
+                ph = ph_next;
+            }
+            if (*abort_flag) {
+                stop = true;
+                break;
+            }
+            mma_commit(acc_full(b));
+            if (b) ++use[1]; else ++use[0];
+            ++j;
+        }
+        // all issued tensor-core work completes before TMEM is released
+        mma_commit(drain_bar);
+        if (!mbar_wait_bounded(drain_bar, 0)) *abort_flag = 1;
     }
+
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) {
-        if (tid == 0) {
-            atomicExch(status, FP4_ERR_TIMEOUT);
-            // give in-flight tensor-core work a last bounded chance to finish
-            mbar_wait_bounded(acc_bar, 0);
-        }
-        __syncthreads();
-    }
+    if (*abort_flag && tid == 0) atomicExch(status, FP4_ERR_TIMEOUT);
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -264,6 +429,78 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
+int sm_count() {
+    static thread_local int device = -1, count = 0;
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return 0;
+    if (d != device) {
+        if (cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+            return 0;
+        device = d;
+    }
+    return count;
+}
+
+// Tensor maps of the activations [total_rows, k] bf16 (64 x 128 boxes, 128-byte
+// swizzle; rows past total_rows and columns past k read as zero) and of the packed
+// weights [experts * n, k / 2] uint8 (32-byte x wrows boxes, no swizzle).
+cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_t *w_packed,
+                             int64_t experts, int64_t n, int64_t k, int wrows, CUtensorMap *map_x,
+                             CUtensorMap *map_w) {
+    EncodeTiled encode = tensor_map_encoder();
+    if (encode == nullptr) return cudaErrorNotSupported;
+    const cuuint32_t elem_strides[2] = {1, 1};
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)(total_rows > 0 ? total_rows : 1)};
+        const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+        const cuuint32_t box[2] = {kK, kXBox};
+        if (encode(map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a), dims,
+                   strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)(experts * n)};
+        const cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+        const cuuint32_t box[2] = {kK / 2, (cuuint32_t)wrows};
+        if (encode(map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_packed), dims,
+                   strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+template <class C>
+cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_t experts,
+                        int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
+                        const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
+                        int32_t *status, cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int device = 0;
+    cudaError_t err = cudaGetDevice(&device);
+    if (err != cudaSuccess) return err;
+    if (configured_device != device) {
+        err = cudaFuncSetAttribute(mx_moe_gemm_kernel<C>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (err != cudaSuccess) return err;
+        configured_device = device;
+    }
+    CUtensorMap map_x, map_w;
+    err = tmem_tensor_maps(a, total_rows, w_packed, experts, n, k, C::kWRows, &map_x, &map_w);
+    if (err != cudaSuccess) return err;
+    const int64_t items = experts * ((max_rows + C::kTok - 1) / C::kTok) *
+                          ((n + C::kWRows - 1) / C::kWRows);
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = (int)(items < sms ? items : sms);
+    mx_moe_gemm_kernel<C><<<grid, kThreads, C::kSmemBytes, stream>>>(
+        map_x, map_w, expert_offsets, w_scales, (int32_t)experts, max_rows, total_rows,
+        (int32_t)n, (int32_t)k, out, status);
+    return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -271,38 +508,11 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
                                int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
                                const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
                                int32_t *status, cudaStream_t stream) {
-    if (mx_moe_gemm_wide_eligible(w_packed, w_scales, n, k))
-        return launch_mx_moe_gemm_wide(a, expert_offsets, experts, max_rows, total_rows, w_packed,
-                                       w_scales, n, k, out, status, stream);
-    static thread_local int configured_device = -1;
-    int device = 0;
-    cudaError_t err = cudaGetDevice(&device);
-    if (err != cudaSuccess) return err;
-    if (configured_device != device) {
-        err = cudaFuncSetAttribute(mx_moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kSmemBytes);
-        if (err != cudaSuccess) return err;
-        configured_device = device;
-    }
-    // TMA descriptor of the activations [total_rows, k] bf16: 64 x 128 boxes with the
-    // 128-byte swizzle; rows past total_rows and columns past k read as zero.
-    EncodeTiled encode = tensor_map_encoder();
-    if (encode == nullptr) return cudaErrorNotSupported;
-    CUtensorMap map;
-    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)(total_rows > 0 ? total_rows : 1)};
-    const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-    const cuuint32_t box[2] = {kTileK, kTileM};
-    const cuuint32_t elem_strides[2] = {1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a), dims, strides,
-               box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((n + kTileN - 1) / kTileN),
-                    (unsigned)((max_rows + kTileM - 1) / kTileM), (unsigned)experts);
-    mx_moe_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-        map, expert_offsets, w_packed, w_scales, max_rows, total_rows, (int32_t)n, (int32_t)k, out,
-        status);
-    return cudaGetLastError();
+    if (max_rows > 128)
+        return launch_tmem<CfgLarge>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
+                                     w_scales, n, k, out, status, stream);
+    return launch_tmem<CfgSmall>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
+                                 w_scales, n, k, out, status, stream);
 }
 
 }  // namespace fp4mx

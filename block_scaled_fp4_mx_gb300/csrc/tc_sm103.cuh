@@ -65,14 +65,63 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+// One K slice of MMAs with A in tensor memory, then a commit to `empty_bar`, with
+// a non-blocking probe of the next stage's barrier (`next_bar`, phase
+// `next_phase`) issued ahead of them so that its latency hides behind the MMA
+// issue. kTiles accumulators (A tiles 32 columns apart, D tiles kN columns
+// apart) each take four K = 16 steps: A advances 8 columns and the B descriptor
+// 32 bytes (2 in its address field) per step. `accumulate` = 0 overwrites D with
+// the first step. Returns whether the probed phase had already completed.
+template <int kTiles, int kN>
+__device__ __forceinline__ uint32_t mma_slice_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t accumulate,
+                                                     uint32_t empty_bar, uint32_t next_bar,
+                                                     uint32_t next_phase) {
+    static_assert(kTiles == 1 || kTiles == 2, "accumulators per slice");
+    uint32_t ready;
+    if constexpr (kTiles == 1) {
+        asm volatile(
+            "{\n\t.reg .pred pr, p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 pr, [%7], %8;\n\t"
+            "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+            "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+            "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %4, pt;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %4, pt;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %4, pt;\n\t"
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+            "selp.u32 %0, 1, 0, pr;\n\t}"
+            : "=r"(ready)
+            : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar),
+              "r"(next_bar), "r"(next_phase)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred pr, p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t"
+            ".reg .b32 a1, a2, a3, a4, a5, a6, a7, d1;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 pr, [%7], %8;\n\t"
+            "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+            "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+            "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
+            "add.u32 a4, %2, 32;\n\tadd.u32 a5, %2, 40;\n\tadd.u32 a6, %2, 48;\n\t"
+            "add.u32 a7, %2, 56;\n\tadd.u32 d1, %1, %9;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %4, pt;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %4, pt;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %4, pt;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a4], %3, %4, p0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a5], b1, %4, pt;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a6], b2, %4, pt;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a7], b3, %4, pt;\n\t"
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+            "selp.u32 %0, 1, 0, pr;\n\t}"
+            : "=r"(ready)
+            : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar),
+              "r"(next_bar), "r"(next_phase), "n"(kN)
+            : "memory");
+    }
+    return ready;
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -97,33 +146,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 consecutive 32-bit columns of this thread's TMEM lane from registers; the
+// stores are complete once tmem_wait_st() returns.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Read-only global loads issued where they stand in the program (volatile asm
 // keeps them ahead of the work that follows), so that prefetched slices really
 // are in flight while earlier slices are decoded.
-__device__ __forceinline__ uint4 ldg_early_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 __device__ __forceinline__ uint32_t ldg_early_u8(const void *p) {
     uint32_t v;
     asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
-}
-
-// 16-byte store to a shared-memory address (always the shared-state space).
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-// Byte offset of 16-byte chunk `kc` (8 bf16 along K) of row `r` in a tile of
-// 128-byte rows with the 128-byte swizzle (chunk index XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t kc) {
-    return r * 128u + ((kc ^ (r & 7u)) << 4);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -147,29 +194,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 }
 
 
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
-// global to shared memory, completing its bytes of transaction count on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)
                  : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 

@@ -101,15 +101,15 @@ def test_moe_gate_up_shape(oracle_impl):
 
 
 @pytest.mark.parametrize("rows,n,k", [([512, 300, 129, 0, 1], 512, 2880), ([256, 255, 257], 288, 704)])
-def test_two_row_tiles_per_cta(oracle_impl, rows, n, k):
-    """More than 128 rows per expert: each CTA owns two 128-row tiles sharing one
-    decoded weight tile; experts whose last tile pair holds one tile or a ragged
-    second tile included."""
+def test_256_token_slabs(oracle_impl, rows, n, k):
+    """More than 128 rows per expert: 256-token slabs against one decoded weight
+    tile; slabs with at most 128 live tokens (N = 128 MMAs), a ragged last slab
+    and an empty expert included."""
     run_case(oracle_impl, rows, n, k, seed=sum(rows) + k)
 
 
-def test_two_row_tiles_rows_beyond_capacity_flagged(oracle_impl):
-    """The capacity check holds for the two-tile kernel as well."""
+def test_256_token_slabs_rows_beyond_capacity_flagged(oracle_impl):
+    """The capacity check holds with 256-token slabs as well."""
     k, n = 64, 64
     offsets = torch.tensor([0, 10, 400], dtype=torch.int64, device=DEV)
     a = torch.zeros(400, k, dtype=torch.bfloat16, device=DEV)
@@ -120,14 +120,14 @@ def test_two_row_tiles_rows_beyond_capacity_flagged(oracle_impl):
     assert int(status.item()) == fp4.Status.ERR_SHAPE
 
 
-def test_general_kernel_large_k(oracle_impl):
-    """k above 4096 takes the general (128 x 128) kernel."""
+def test_large_k(oracle_impl):
+    """A long reduction: k = 4160, 65 slices of 64."""
     run_case(oracle_impl, [40, 130], 160, 4096 + 64, seed=11)
 
 
-def test_general_kernel_unaligned_scales(oracle_impl):
-    """Scales that are not 16-byte aligned also take the general kernel; the result
-    must not depend on which kernel ran."""
+def test_unaligned_scales(oracle_impl):
+    """Scale buffers at an odd byte address give the same result as aligned ones
+    (the E8M0 bytes are read with byte loads)."""
     rows, n, k = [96, 33], 320, 1024
     offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
     rng = np.random.default_rng(12)
@@ -141,13 +141,14 @@ def test_general_kernel_unaligned_scales(oracle_impl):
     scales_even = torch.from_numpy(scales_host).to(DEV)
     a_t = torch.from_numpy(a_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
     off_t = torch.from_numpy(offsets).to(DEV)
-    out_general, st1 = fp4.fp4_mx_moe_gemm(a_t, off_t, packed, scales_odd, 96)
-    out_wide, st2 = fp4.fp4_mx_moe_gemm(a_t, off_t, packed, scales_even, 96)
+    out_odd, st1 = fp4.fp4_mx_moe_gemm(a_t, off_t, packed, scales_odd, 96)
+    out_even, st2 = fp4.fp4_mx_moe_gemm(a_t, off_t, packed, scales_even, 96)
     torch.cuda.synchronize()
     assert int(st1.item()) == 0 and int(st2.item()) == 0
     exact, absdot = oracle_impl.mx_moe_gemm(a_bits, offsets, w.packed.reshape(2, n, k // 2),
                                             scales_host)
-    for got in (out_general, out_wide):
+    assert torch.equal(out_odd.view(torch.int16), out_even.view(torch.int16))
+    for got in (out_odd, out_even):
         g = got.float().cpu().numpy().astype(np.float64)
         assert np.all(np.abs(g - exact) <= tolerance(exact, absdot, k))
 
