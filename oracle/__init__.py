@@ -26,6 +26,9 @@ Functions and the passages they follow (web pages cited by title and section):
   pull 51583", the unpack_B loop of the CPU MoE GEMM): per expert, activations
   times the unpacked weights transposed, exact in float64 (numpy matmul as the
   step), with the sum of |a||w| that bounds fp32 accumulation error.
+* ``mx_moe_forward`` -- the MoE layer around that GEMM (same page: the CPU test of
+  ops.fused_experts_cpu with MXFP4 experts): gate/up GEMM, silu(gate) * up, down
+  GEMM, top-k weighted sum, exact in float64 with its intermediates.
 * ``nv_dequant`` -- the same NVFP4 element rule over every row of a table (the
   dense dequant a tied lm_head needs; same page, "Comments" and "Risks").
 * ``nv_embedding_gather`` / ``nv_embedding_gather_at`` -- NVFP4 gather-dequant,
@@ -255,6 +258,63 @@ class Oracle:
             out[r0:r1] = a[r0:r1] @ w.T
             absdot[r0:r1] = np.abs(a[r0:r1]) @ np.abs(w).T
         return out, absdot
+
+    def mx_moe_forward(self, a_bits, topk_ids, topk_weights, w1_packed, w1_scales, w2_packed,
+                       w2_scales, threads: int = 1) -> dict:
+        """The MoE layer the unpack feeds ("vllm-project/vllm pull 51583": the test that
+        runs ops.fused_experts_cpu with MXFP4 experts, and the zero-code test whose
+        comment says silu(0) * 0 = 0 collapses the whole layer to exact zeros). For
+        token m and each of its top-k slots j, with expert e = topk_ids[m, j] and
+        weight w = topk_weights[m, j]:
+            h   = a[m] @ W1_e^T            W1_e [2N, K] unpacked (gate rows, then up rows)
+            act = silu(h[:N]) * h[N:]      silu(x) = x / (1 + exp(-x))
+            y   = act @ W2_e^T             W2_e [K, N] unpacked
+            out[m] += w * y
+        all in float64 with no intermediate rounding (bf16 x bf16 products are exact,
+        the sums far more precise than the fp32 work they are compared with). A slot
+        whose expert id is outside [0, E) contributes nothing and is counted.
+
+        Returns a dict: out [M, K]; the per-slot g, u, act [M, topk, N] and y
+        [M, topk, K]; sg, su [M, topk, N] = sums of |a||w1| behind g and u; the
+        unpacked weights w1 [E, 2N, K], w2 [E, K, N] (float64); bad (count)."""
+        a = self.bf16_to_f64(a_bits)
+        ids = np.asarray(topk_ids, dtype=np.int64)
+        wts = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
+        m_tok, k = a.shape
+        topk = ids.shape[1]
+        experts, two_n, half_k = w1_packed.shape
+        n = two_n // 2
+        if 2 * half_k != k or w2_packed.shape != (experts, k, n // 2):
+            raise ValueError("inconsistent MoE shapes")
+        w1 = np.stack([self.bf16_to_f64(self.mx_unpack(w1_packed[e], w1_scales[e], threads))
+                       .reshape(two_n, k) for e in range(experts)]) if experts else np.zeros((0, two_n, k))
+        w2 = np.stack([self.bf16_to_f64(self.mx_unpack(w2_packed[e], w2_scales[e], threads))
+                       .reshape(k, n) for e in range(experts)]) if experts else np.zeros((0, k, n))
+        g = np.zeros((m_tok, topk, n))
+        u = np.zeros((m_tok, topk, n))
+        sg = np.zeros((m_tok, topk, n))
+        su = np.zeros((m_tok, topk, n))
+        act = np.zeros((m_tok, topk, n))
+        y = np.zeros((m_tok, topk, k))
+        out = np.zeros((m_tok, k))
+        bad = int(np.count_nonzero((ids < 0) | (ids >= experts)))
+        for e in range(experts):
+            ms, js = np.nonzero(ids == e)
+            if ms.size == 0:
+                continue
+            rows = a[ms]
+            h = rows @ w1[e].T
+            habs = np.abs(rows) @ np.abs(w1[e]).T
+            g[ms, js], u[ms, js] = h[:, :n], h[:, n:]
+            sg[ms, js], su[ms, js] = habs[:, :n], habs[:, n:]
+            with np.errstate(over="ignore"):
+                act_e = h[:, :n] / (1.0 + np.exp(-h[:, :n])) * h[:, n:]
+            act[ms, js] = act_e
+            y_e = act_e @ w2[e].T
+            y[ms, js] = y_e
+            np.add.at(out, ms, wts[ms, js][:, None] * y_e)
+        return {"out": out, "g": g, "u": u, "sg": sg, "su": su, "act": act, "y": y,
+                "w1": w1, "w2": w2, "bad": bad}
 
     # -- NVFP4 ----------------------------------------------------------------
     def nv_embedding_gather(self, ids, weight, scales, global_scale, group_size: int = 16,

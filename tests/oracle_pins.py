@@ -452,6 +452,99 @@ def pin_moe_gemm_brute_force(o):
 
 
 # ---------------------------------------------------------------------------
+# pins: the MoE layer (gate/up GEMM, silu(gate) * up, down GEMM, top-k sum)
+# ---------------------------------------------------------------------------
+
+def pin_moe_forward_zero_codes_collapse(o):
+    """The pages' zero-code MoE test ("vllm-project/vllm pull 51583", the test with
+    N = K = 64, E = 2, M = 4): gate/up weights made only of one zero code at any
+    E8M0 give silu(0) * 0 = 0 in every slot, so the whole layer must be exactly 0
+    whatever the (nonzero) down weights are."""
+    n, k, experts, m_tok = 64, 64, 2, 4
+    rng = np.random.default_rng(91)
+    a_bits = _bf16_bits(rng.standard_normal((m_tok, k)))
+    w2 = inputs.mx_random(experts * k, n, seed=92, e_lo=118, e_hi=126)
+    w2p, w2s = w2.packed.reshape(experts, k, n // 2), w2.scales.reshape(experts, k, n // 32)
+    for zero_byte in (0x00, 0x88, 0x08, 0x80):
+        for e8m0 in (0, 1, 127, 200, 254, 255):
+            w1p = np.full((experts, 2 * n, k // 2), zero_byte, dtype=np.uint8)
+            w1s = np.full((experts, 2 * n, k // 32), e8m0, dtype=np.uint8)
+            r = o.mx_moe_forward(a_bits, np.zeros((m_tok, 1), np.int64),
+                                 np.ones((m_tok, 1), np.float32), w1p, w1s, w2p, w2s)
+            assert np.all(r["out"] == 0.0), (zero_byte, e8m0)
+
+
+def pin_moe_forward_brute_force(o):
+    """A tiny layer against plain scalar loops over the decoded codes (gate rows
+    first, silu(x) = x / (1 + e^-x), both GEMMs, the weighted top-k sum)."""
+    import math
+    rng = np.random.default_rng(93)
+    m_tok, k, n, experts, topk = 3, 32, 32, 3, 2
+    a_vals = rng.integers(-6, 7, size=(m_tok, k)) / 8.0
+    a_bits = _bf16_bits(a_vals)
+    ids = np.array([[0, 2], [1, 1], [2, 0]])
+    wts = np.array([[0.25, 0.75], [0.5, 0.125], [1.0, -0.5]], dtype=np.float32)
+    w1 = inputs.mx_random(experts * 2 * n, k, seed=94, e_lo=123, e_hi=127)
+    w2 = inputs.mx_random(experts * k, n, seed=95, e_lo=123, e_hi=127)
+    r = o.mx_moe_forward(a_bits, ids, wts, w1.packed.reshape(experts, 2 * n, k // 2),
+                         w1.scales.reshape(experts, 2 * n, k // 32),
+                         w2.packed.reshape(experts, k, n // 2), w2.scales.reshape(experts, k, n // 32))
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    c1 = nibble_codes(w1.packed).reshape(experts, 2 * n, k)
+    c2 = nibble_codes(w2.packed).reshape(experts, k, n)
+    s1 = w1.scales.reshape(experts, 2 * n, k // 32)
+    s2 = w2.scales.reshape(experts, k, n // 32)
+
+    def val(c, e8m0):
+        c = int(c)
+        return (-1.0 if c & 8 else 1.0) * mags[c & 7] * 2.0 ** (int(e8m0) - 127)
+
+    for m in range(m_tok):
+        expect = [0.0] * k
+        for j in range(topk):
+            e = int(ids[m, j])
+            hid = []
+            for i in range(n):
+                gate = sum(a_vals[m, kk] * val(c1[e, i, kk], s1[e, i, kk // 32]) for kk in range(k))
+                up = sum(a_vals[m, kk] * val(c1[e, n + i, kk], s1[e, n + i, kk // 32]) for kk in range(k))
+                hid.append(gate / (1.0 + math.exp(-gate)) * up)
+            for c in range(k):
+                yc = sum(hid[i] * val(c2[e, c, i], s2[e, c, i // 32]) for i in range(n))
+                expect[c] += float(wts[m, j]) * yc
+        got = r["out"][m]
+        assert np.allclose(got, expect, rtol=1e-12, atol=1e-12 * max(1.0, max(map(abs, expect)))), m
+
+
+def pin_moe_forward_routing_invariants(o):
+    """Permuting tokens permutes the output rows; a slot whose expert id is out of
+    range adds nothing (and is counted); two slots on one expert add up like one
+    slot with the summed weight."""
+    rng = np.random.default_rng(96)
+    m_tok, k, n, experts = 5, 64, 32, 3
+    a_bits = _bf16_bits(rng.standard_normal((m_tok, k)))
+    w1 = inputs.mx_random(experts * 2 * n, k, seed=97, e_lo=120, e_hi=126)
+    w2 = inputs.mx_random(experts * k, n, seed=98, e_lo=120, e_hi=126)
+    wp = (w1.packed.reshape(experts, 2 * n, k // 2), w1.scales.reshape(experts, 2 * n, k // 32),
+          w2.packed.reshape(experts, k, n // 2), w2.scales.reshape(experts, k, n // 32))
+    ids = np.array([[0, 1], [2, 2], [1, 0], [0, 2], [2, 1]])
+    wts = np.array([[0.5, 0.5], [0.25, 0.5], [1.0, 0.0], [0.75, 0.125], [0.5, 0.25]], np.float32)
+    base = o.mx_moe_forward(a_bits, ids, wts, *wp)
+    perm = np.array([3, 0, 4, 1, 2])
+    r = o.mx_moe_forward(a_bits[perm], ids[perm], wts[perm], *wp)
+    assert np.array_equal(r["out"], base["out"][perm])
+    bad_ids = ids.copy()
+    bad_ids[1, 0] = experts
+    bad_ids[4, 1] = -1
+    r = o.mx_moe_forward(a_bits, bad_ids, wts, *wp)
+    assert r["bad"] == 2
+    ref = o.mx_moe_forward(a_bits, bad_ids.clip(0, experts - 1),
+                           np.where((bad_ids < 0) | (bad_ids >= experts), 0.0, wts).astype(np.float32), *wp)
+    assert np.array_equal(r["out"], ref["out"])
+    one = o.mx_moe_forward(a_bits[1:2], np.array([[2]]), np.array([[0.75]], np.float32), *wp)
+    assert np.allclose(base["out"][1], one["out"][0], rtol=1e-14, atol=0)
+
+
+# ---------------------------------------------------------------------------
 # pins: NVFP4
 # ---------------------------------------------------------------------------
 

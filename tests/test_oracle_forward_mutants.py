@@ -1,0 +1,62 @@
+"""Plant plausible mistakes in a copy of the oracle's MoE-layer function (its
+Python source, rewritten and re-executed; the real oracle is untouched) and check
+that the MoE-layer pins catch each one (CPU only)."""
+import inspect
+import textwrap
+import warnings
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTATIONS = [
+    ("act_e = h[:, :n] / (1.0 + np.exp(-h[:, :n])) * h[:, n:]",
+     "act_e = h[:, n:] / (1.0 + np.exp(-h[:, n:])) * h[:, :n]", "gate and up rows swapped"),
+    ("act_e = h[:, :n] / (1.0 + np.exp(-h[:, :n])) * h[:, n:]",
+     "act_e = 1.0 / (1.0 + np.exp(-h[:, :n])) * h[:, n:]", "sigmoid instead of silu"),
+    ("act_e = h[:, :n] / (1.0 + np.exp(-h[:, :n])) * h[:, n:]",
+     "act_e = h[:, :n] / (1.0 + np.exp(h[:, :n])) * h[:, n:]", "silu with the wrong sign"),
+    ("act_e = h[:, :n] / (1.0 + np.exp(-h[:, :n])) * h[:, n:]",
+     "act_e = np.maximum(h[:, :n], 0.0) * h[:, n:]", "relu instead of silu"),
+    ("np.add.at(out, ms, wts[ms, js][:, None] * y_e)", "np.add.at(out, ms, y_e)",
+     "top-k weights dropped"),
+    ("np.add.at(out, ms, wts[ms, js][:, None] * y_e)", "out[ms] = wts[ms, js][:, None] * y_e",
+     "slots of one token overwrite instead of add"),
+    ("h = rows @ w1[e].T", "h = rows @ w1[(e + 1) % experts].T", "another expert's gate/up weights"),
+    ("y_e = act_e @ w2[e].T", "y_e = act_e @ w2[(e + 1) % experts].T", "another expert's down weights"),
+    (".reshape(k, n) for e in range(experts)]", ".reshape(n, k).T for e in range(experts)]",
+     "down weights read transposed"),
+    ("bad = int(np.count_nonzero((ids < 0) | (ids >= experts)))",
+     "bad = int(np.count_nonzero((ids < 0) | (ids > experts)))", "last valid id off by one"),
+]
+
+FORWARD_PINS = [p for p in oracle_pins.ALL_PINS if p.__name__.startswith("pin_moe_forward")]
+
+
+def _source():
+    return textwrap.dedent(inspect.getsource(oracle.Oracle.mx_moe_forward))
+
+
+def test_mutations_apply():
+    src = _source()
+    for before, _, what in MUTATIONS:
+        assert src.count(before) >= 1, what
+
+
+@pytest.mark.parametrize("before,after,what", MUTATIONS, ids=[m[2] for m in MUTATIONS])
+def test_forward_pins_catch_mutant(before, after, what):
+    namespace = dict(vars(oracle))
+    exec(compile(_source().replace(before, after, 1), "<mutant>", "exec"), namespace)
+    mutant_cls = type("MutantOracle", (oracle.Oracle,), {"mx_moe_forward": namespace["mx_moe_forward"]})
+    mutant = mutant_cls(oracle.lib())
+    failed = []
+    with warnings.catch_warnings():
+        warnings.simplefilter("ignore", RuntimeWarning)
+        for pin in FORWARD_PINS:
+            try:
+                pin(mutant)
+            except (AssertionError, ValueError, IndexError):
+                failed.append(pin.__name__)
+    assert failed, f"no pin caught the mutant: {what}"
