@@ -49,7 +49,7 @@ UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("step", "mx_moe", "mx_stress", "mx_exhaustive", "nv_embedding_200k",
              "nv_embedding_32k", "nv_dequant_200k", "nv_dequant_32k", "mx_quantize_moe",
-             "mx_moe_gemm_128", "mx_moe_gemm_512", "kv_pages")
+             "mx_moe_gemm_128", "mx_moe_gemm_512", "mx_moe_forward", "kv_pages")
 
 
 # ---------------------------------------------------------------------------
@@ -443,6 +443,9 @@ class MoeGemmOp:
         fp4.fp4_mx_moe_gemm(self.a, self.off, self.wp, self.ws, self.rows, out=self.o,
                             status=self.status, stream=stream)
 
+    unfused_what = ("fp4_mx_unpack of the weights to bf16 + cuBLAS batched bf16 GEMM "
+                    "(torch.bmm), same inputs")
+
     def unfused(self, torch, fp4, stream):
         """The two-step path for comparison: fp4_mx_unpack of all expert weights to
         bf16 in HBM, then a cuBLAS batched bf16 GEMM."""
@@ -475,6 +478,114 @@ class MoeGemmOp:
         return f"experts of the MoE GEMM ({self.rows} tokens each)"
 
 
+class MoeForwardOp:
+    """fp4_mx_moe_forward: the whole MoE layer (routing, gate/up GEMM with
+    silu(gate) * up, down GEMM, top-k weighted sum) on the MoE weights: 4,096 tokens,
+    top-4 of 32 experts, hidden 2,880, intermediate 2,880."""
+    kind, kernel = "mx_moe_forward", "mx_moe_forward (all kernels)"
+
+    def __init__(self, w1, w2, tokens: int = 4096, topk: int = 4, seed: int = 9):
+        from block_scaled_fp4_mx_gb300 import inputs
+        self.experts = 32
+        self.n2, self.k = w1.rows // self.experts, w1.k  # 2N, K
+        self.n = self.n2 // 2
+        assert w2.rows // self.experts == self.k and w2.k == self.n
+        self.w1, self.w2, self.tokens, self.topk = w1, w2, tokens, topk
+        rng = np.random.default_rng(seed)
+        self.a_bits = inputs.bf16_normal_bits(rng, tokens * self.k, scale=1.0).reshape(tokens, self.k)
+        self.ids = np.stack([rng.permutation(self.experts)[:topk] for _ in range(tokens)]).astype(np.int32)
+        wts = rng.random((tokens, topk)).astype(np.float32)
+        self.wts = (wts / wts.sum(axis=1, keepdims=True)).astype(np.float32)
+        slots = tokens * topk
+        self.elems = w1.n_elems + w2.n_elems  # every expert weight decoded (at least once)
+        self.flops = 2.0 * slots * (self.n2 * self.k + self.k * self.n)
+        self.out_bytes = 2 * tokens * self.k
+        self.bytes = (w1.packed.size + w1.scales.size + w2.packed.size + w2.scales.size
+                      + 2 * tokens * self.k + 8 * slots + self.out_bytes)
+        self.min_bytes = self.bytes
+        self.units, self.elems_per_unit = self.experts, self.elems // self.experts
+
+    def to_device(self, torch, dev):
+        import block_scaled_fp4_mx_gb300 as fp4
+        e, k, n, n2 = self.experts, self.k, self.n, self.n2
+        self.a = torch.from_numpy(self.a_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.t_ids = torch.from_numpy(self.ids).to(dev)
+        self.t_wts = torch.from_numpy(self.wts).to(dev)
+        self.w1p = torch.from_numpy(self.w1.packed.reshape(e, n2, k // 2)).to(dev)
+        self.w1s = torch.from_numpy(self.w1.scales.reshape(e, n2, k // 32)).to(dev)
+        self.w2p = torch.from_numpy(self.w2.packed.reshape(e, k, n // 2)).to(dev)
+        self.w2s = torch.from_numpy(self.w2.scales.reshape(e, k, n // 32)).to(dev)
+        need = fp4.fp4_mx_moe_workspace_bytes(self.tokens, self.topk, e, n, k)
+        self.work = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.o = torch.empty(self.tokens, k, dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch(self, fp4, stream):
+        fp4.fp4_mx_moe_forward(self.a, self.t_ids, self.t_wts, self.w1p, self.w1s, self.w2p,
+                               self.w2s, out=self.o, workspace=self.work, status=self.status,
+                               stream=stream)
+
+    cpu_start_units = 1  # one expert of the oracle layer is already a few seconds
+    unfused_what = ("fp4_mx_unpack of both weight stacks to bf16 + per-expert cuBLAS GEMMs, "
+                    "torch silu * mul and index_add top-k sum (slot sort precomputed), same inputs")
+
+    def unfused(self, torch, fp4, stream):
+        """The same layer from fp4_mx_unpack of both weight stacks to bf16 in HBM and
+        torch ops (cuBLAS GEMMs per expert, silu * mul, index_add for the top-k sum);
+        the slot sort is done once, outside the timed region."""
+        e, k, n, n2 = self.experts, self.k, self.n, self.n2
+        if not hasattr(self, "w1_bf16"):
+            dev = self.a.device
+            self.w1_bf16 = torch.empty(e, n2, k, dtype=torch.bfloat16, device=dev)
+            self.w2_bf16 = torch.empty(e, k, n, dtype=torch.bfloat16, device=dev)
+            flat = self.ids.reshape(-1)
+            order = np.argsort(flat, kind="stable")
+            self.u_tok = torch.from_numpy(order // self.topk).to(dev)
+            self.u_w = torch.from_numpy(self.wts.reshape(-1)[order]).to(dev)
+            self.u_off = np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=e))])
+            self.u_y = torch.empty(flat.size, k, dtype=torch.bfloat16, device=dev)
+        fp4.fp4_mx_unpack(self.w1p, self.w1s, out=self.w1_bf16, stream=stream)
+        fp4.fp4_mx_unpack(self.w2p, self.w2s, out=self.w2_bf16, stream=stream)
+        xg = self.a.index_select(0, self.u_tok)
+        for x in range(e):
+            r0, r1 = int(self.u_off[x]), int(self.u_off[x + 1])
+            if r1 > r0:
+                h = xg[r0:r1] @ self.w1_bf16[x].T
+                act = torch.nn.functional.silu(h[:, :n]) * h[:, n:]
+                torch.matmul(act, self.w2_bf16[x].T, out=self.u_y[r0:r1])
+        out = torch.zeros(self.tokens, k, dtype=torch.float32, device=self.a.device)
+        out.index_add_(0, self.u_tok, self.u_y.float() * self.u_w[:, None])
+        self.o.copy_(out)
+
+    def e2e_jobs(self, torch, fp4, chunks):
+        ha = torch.from_numpy(self.a_bits.view(np.int16)).pin_memory().view(torch.bfloat16)
+        hi = torch.from_numpy(self.ids).pin_memory()
+        hw = torch.from_numpy(self.wts).pin_memory()
+        ho = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+
+        def fn(st):
+            self.a.copy_(ha, non_blocking=True)
+            self.t_ids.copy_(hi, non_blocking=True)
+            self.t_wts.copy_(hw, non_blocking=True)
+            self.launch(fp4, st)
+            ho.copy_(self.o, non_blocking=True)
+        return [(ha.numel() * 2 + hi.numel() * 4 + hw.numel() * 4, ho.numel() * 2, fn)]
+
+    def oracle_units(self, o, n, threads):
+        """The layer restricted to the first n experts (slots on other experts are
+        dropped): decode and GEMM work both scale with n."""
+        e, k, nn, n2 = self.experts, self.k, self.n, self.n2
+        ids = np.where(self.ids < n, self.ids, -1)
+        o.mx_moe_forward(self.a_bits, ids, self.wts,
+                         self.w1.packed.reshape(e, n2, k // 2)[:n], self.w1.scales.reshape(e, n2, k // 32)[:n],
+                         self.w2.packed.reshape(e, k, nn // 2)[:n], self.w2.scales.reshape(e, k, nn // 32)[:n],
+                         threads)
+
+    def sample_name(self):
+        return (f"experts of the MoE layer ({self.tokens} tokens, top-{self.topk}; "
+                "slots on other experts dropped)")
+
+
 def load_workload(name: str):
     """The ops of one step of the named workload, in launch order."""
     from block_scaled_fp4_mx_gb300 import inputs
@@ -492,6 +603,7 @@ def load_workload(name: str):
         "kv_pages": lambda: [MxPagesOp(inputs.kv_pages())],
         "mx_moe_gemm_128": lambda: [MoeGemmOp(inputs.mx_moe()[0], 128)],
         "mx_moe_gemm_512": lambda: [MoeGemmOp(inputs.mx_moe()[0], 512)],
+        "mx_moe_forward": lambda: [MoeForwardOp(*inputs.mx_moe())],
     }
     return table[name]()
 
@@ -666,8 +778,7 @@ def run_ours(args, d: Dist):
         comparison = {"unfused_ms_per_step": ms_unfused,
                       "fused_ms_per_step": elapsed_ms / k,
                       "speedup": ms_unfused / (elapsed_ms / k),
-                      "what": "fp4_mx_unpack of the weights to bf16 + cuBLAS batched bf16 GEMM "
-                              "(torch.bmm), same inputs"}
+                      "what": " + ".join(dict.fromkeys(op.unfused_what for op in ops))}
         for op in ops:
             op.launch(fp4, stream)  # leave the fused result in place
         torch.cuda.synchronize()
@@ -777,7 +888,7 @@ def cpu_rates(ops, seconds: float):
     rates, desc = {}, []
     for kind in dict.fromkeys(op.kind for op in ops):
         op = next(p for p in ops if p.kind == kind)
-        n = max(1, min(op.units, 16))
+        n = max(1, min(op.units, getattr(op, "cpu_start_units", 16)))
         while True:
             t = time.perf_counter()
             op.oracle_units(o, n, threads)

@@ -31,6 +31,7 @@ from __future__ import annotations
 from ._lib import Status, last_error, library_path, load, status_string  # noqa: F401
 
 __all__ = ["fp4_mx_unpack", "fp4_mx_unpack_pages", "fp4_mx_quantize", "fp4_mx_moe_gemm",
+           "fp4_mx_moe_forward", "fp4_mx_moe_workspace_bytes",
            "fp4_nv_embedding_gather",
            "fp4_nv_dequant",
            "fp4_status_string",
@@ -249,6 +250,66 @@ def fp4_mx_moe_gemm(a, expert_offsets, w_packed, w_scales, max_rows_per_expert: 
                                   _ptr(status), _stream_handle(stream, a.device))
     if code != Status.OK:
         raise Fp4Error("fp4_mx_moe_gemm", code)
+    return out, status
+
+
+def fp4_mx_moe_workspace_bytes(tokens: int, topk: int, experts: int, n: int, k: int) -> int:
+    """Bytes of device workspace fp4_mx_moe_forward needs (raises on invalid sizes)."""
+    size = load().fp4_mx_moe_workspace_bytes(int(tokens), int(topk), int(experts), int(n), int(k))
+    if size < 0:
+        raise ValueError("invalid MoE layer sizes")
+    return int(size)
+
+
+def fp4_mx_moe_forward(a, topk_ids, topk_weights, w1_packed, w1_scales, w2_packed, w2_scales,
+                       max_rows_per_expert=None, out=None, workspace=None, status=None,
+                       stream=None):
+    """The MoE layer with MXFP4 experts: ``a`` bf16 [M, k], ``topk_ids`` int32 [M, topk],
+    ``topk_weights`` fp32 [M, topk], ``w1_*`` [E, 2n, k/2] / [E, 2n, k/32] (gate rows
+    then up rows), ``w2_*`` [E, k, n/2] / [E, k, n/32] -> bf16 [M, k]:
+    out[m] = sum_j w[m, j] * (silu(gate) * up) @ W2_e^T. ``max_rows_per_expert``
+    defaults to M (enough whenever no token repeats an expert among its slots);
+    ``workspace`` (uint8 CUDA tensor, allocated if None) must hold
+    fp4_mx_moe_workspace_bytes(M, topk, E, n, k) bytes. Returns (out, status)."""
+    torch = _torch()
+    _check_cuda(a, "a", (torch.bfloat16, torch.int16, torch.uint16))
+    _check_cuda(topk_ids, "topk_ids", (torch.int32,))
+    _check_cuda(topk_weights, "topk_weights", (torch.float32,))
+    for t, name in ((w1_packed, "w1_packed"), (w1_scales, "w1_scales"), (w2_packed, "w2_packed"),
+                    (w2_scales, "w2_scales")):
+        _check_cuda(t, name, (torch.uint8,))
+    if a.dim() != 2 or topk_ids.dim() != 2 or w1_packed.dim() != 3 or w2_packed.dim() != 3:
+        raise ValueError("a [M, k], topk_ids [M, topk], w1_packed [E, 2n, k/2], w2_packed [E, k, n/2]")
+    tokens, k = a.shape
+    topk = topk_ids.shape[1]
+    experts, two_n, half_k = w1_packed.shape
+    n = two_n // 2
+    if (2 * half_k != k or two_n % 2 or topk_ids.shape[0] != tokens
+            or tuple(topk_weights.shape) != tuple(topk_ids.shape)
+            or tuple(w1_scales.shape) != (experts, two_n, k // 32)
+            or tuple(w2_packed.shape) != (experts, k, n // 2)
+            or tuple(w2_scales.shape) != (experts, k, n // 32)):
+        raise ValueError("inconsistent MoE layer shapes")
+    need = fp4_mx_moe_workspace_bytes(tokens, topk, experts, n, k)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    _check_cuda(workspace, "workspace", (torch.uint8,))
+    if out is None:
+        out = torch.empty((tokens, k), dtype=torch.bfloat16, device=a.device)
+    _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
+    if tuple(out.shape) != (tokens, k):
+        raise ValueError(f"out must have shape {(tokens, k)}")
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=a.device)
+    _check_cuda(status, "status", (torch.int32,))
+    max_rows = tokens if max_rows_per_expert is None else int(max_rows_per_expert)
+    code = load().fp4_mx_moe_forward(
+        _ptr(a), _ptr(topk_ids), _ptr(topk_weights), tokens, topk, experts, max_rows,
+        _ptr(w1_packed), _ptr(w1_scales), _ptr(w2_packed), _ptr(w2_scales), n, k,
+        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(status),
+        _stream_handle(stream, a.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_mx_moe_forward", code)
     return out, status
 
 

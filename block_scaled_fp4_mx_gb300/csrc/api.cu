@@ -232,6 +232,74 @@ FP4_EXPORT fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *exp
     return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_moe_gemm launch");
 }
 
+namespace {
+
+// Shape rules of the MoE layer entry points (see include/fp4mx.h).
+bool moe_shape_ok(int64_t tokens, int64_t topk, int64_t experts, int64_t n, int64_t k) {
+    if (tokens < 0 || topk < 1 || topk > 1024 || experts < 1 || experts > 65535 || n < 32 ||
+        k < 32 || n % 32 != 0 || k % 32 != 0 || n > (1ll << 20) || k > (1ll << 20))
+        return false;
+    return tokens <= INT32_MAX / topk;  // slot and row indices are int32
+}
+
+}  // namespace
+
+FP4_EXPORT int64_t fp4_mx_moe_workspace_bytes(int64_t tokens, int64_t topk, int64_t experts,
+                                              int64_t n, int64_t k) {
+    if (!moe_shape_ok(tokens, topk, experts, n, k)) return -1;
+    return (int64_t)fp4mx::moe_workspace_layout(tokens, topk, experts, n, k).total;
+}
+
+FP4_EXPORT fp4_status fp4_mx_moe_forward(const uint16_t *a_bf16, const int32_t *topk_ids,
+                                         const float *topk_weights, int64_t tokens, int64_t topk,
+                                         int64_t experts, int64_t max_rows_per_expert,
+                                         const uint8_t *w1_packed, const uint8_t *w1_scales_e8m0,
+                                         const uint8_t *w2_packed, const uint8_t *w2_scales_e8m0,
+                                         int64_t n, int64_t k, void *workspace,
+                                         int64_t workspace_bytes, uint16_t *out_bf16,
+                                         int32_t *status, fp4_stream_t stream) {
+    clear_error();
+    if (!moe_shape_ok(tokens, topk, experts, n, k) || max_rows_per_expert < 0) return FP4_ERR_SHAPE;
+    if (tokens == 0) return FP4_OK;
+    const int64_t pairs = tokens * topk;
+    const int64_t max_rows = max_rows_per_expert < pairs ? max_rows_per_expert : pairs;
+    if (a_bf16 == nullptr || topk_ids == nullptr || topk_weights == nullptr || w1_packed == nullptr ||
+        w1_scales_e8m0 == nullptr || w2_packed == nullptr || w2_scales_e8m0 == nullptr ||
+        workspace == nullptr || out_bf16 == nullptr || status == nullptr)
+        return FP4_ERR_NULL_PTR;
+    if (misaligned(a_bf16, 16) || misaligned(w1_packed, 16) || misaligned(w2_packed, 16) ||
+        misaligned(out_bf16, 16) || misaligned(workspace, 256) || misaligned(topk_ids, 4) ||
+        misaligned(topk_weights, 4) || misaligned(status, 4))
+        return FP4_ERR_ALIGN;
+    const uint64_t need = fp4mx::moe_workspace_layout(tokens, topk, experts, n, k).total;
+    if (workspace_bytes < 0 || (uint64_t)workspace_bytes < need) {
+        std::snprintf(g_last_error, sizeof g_last_error,
+                      "workspace of %lld bytes, the layer needs %llu", (long long)workspace_bytes,
+                      (unsigned long long)need);
+        return FP4_ERR_SHAPE;
+    }
+    const uint64_t out_bytes = (uint64_t)tokens * (uint64_t)k * 2;
+    const uint64_t w1_bytes = (uint64_t)experts * 2 * (uint64_t)n * (uint64_t)k / 2;
+    const uint64_t w2_bytes = (uint64_t)experts * (uint64_t)k * (uint64_t)n / 2;
+    const void *inputs[] = {a_bf16, topk_ids, topk_weights, w1_packed, w1_scales_e8m0, w2_packed,
+                            w2_scales_e8m0, status};
+    const uint64_t in_bytes[] = {out_bytes, (uint64_t)pairs * 4, (uint64_t)pairs * 4, w1_bytes,
+                                 w1_bytes / 16, w2_bytes, w2_bytes / 16, 4};
+    for (int i = 0; i < 8; ++i)
+        if (overlaps(out_bf16, out_bytes, inputs[i], in_bytes[i]) ||
+            overlaps(workspace, need, inputs[i], in_bytes[i]))
+            return FP4_ERR_ALIAS;
+    if (overlaps(out_bf16, out_bytes, workspace, need)) return FP4_ERR_ALIAS;
+    const void *ptrs[] = {a_bf16, topk_ids, topk_weights, w1_packed, w1_scales_e8m0, w2_packed,
+                          w2_scales_e8m0, workspace, out_bf16, status};
+    const fp4_status s = check_pointers(ptrs, 10);
+    if (s != FP4_OK) return s;
+    const cudaError_t err = fp4mx::launch_mx_moe_forward(
+        a_bf16, topk_ids, topk_weights, tokens, topk, experts, max_rows, w1_packed, w1_scales_e8m0,
+        w2_packed, w2_scales_e8m0, n, k, workspace, out_bf16, status, (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_moe_forward launch");
+}
+
 FP4_EXPORT fp4_status fp4_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,
                                           const uint8_t *packed_pool,
                                           const uint8_t *scales_pool_e8m0, int64_t pool_pages,
@@ -316,4 +384,4 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 104; }
+FP4_EXPORT int fp4_abi_version(void) { return 105; }

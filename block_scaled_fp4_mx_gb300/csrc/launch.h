@@ -35,6 +35,28 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
                                const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
                                int32_t *status, cudaStream_t stream);
 
+// The MoE layer's gate/up GEMM: x [total_rows, k] against w1 [experts, 2n, k/2]
+// (gate rows 0..n-1, up rows n..2n-1 of each expert) -> act [total_rows, n] =
+// bf16(silu(gate) * up).
+cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offsets, int64_t experts,
+                                  int64_t max_rows, int64_t total_rows, const uint8_t *w1_packed,
+                                  const uint8_t *w1_scales, int64_t n, int64_t k, uint16_t *act,
+                                  int32_t *status, cudaStream_t stream);
+
+// The MoE layer: routing, gate/up GEMM with silu(gate) * up, down GEMM, top-k
+// weighted sum. Byte offsets of its scratch arrays in the caller's workspace.
+struct MoeWorkspace {
+    uint64_t counts, cursors, offsets, pos, xg, act, y, total;
+};
+MoeWorkspace moe_workspace_layout(int64_t tokens, int64_t topk, int64_t experts, int64_t n,
+                                  int64_t k);
+cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
+                                  const float *topk_weights, int64_t tokens, int64_t topk,
+                                  int64_t experts, int64_t max_rows, const uint8_t *w1_packed,
+                                  const uint8_t *w1_scales, const uint8_t *w2_packed,
+                                  const uint8_t *w2_scales, int64_t n, int64_t k, void *workspace,
+                                  uint16_t *out, int32_t *status, cudaStream_t stream);
+
 // Paged MXFP4 dequant: num_pages (> 0) pages of page_elems (a positive multiple of
 // 32) codes gathered from a pool by id.
 cudaError_t launch_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,

@@ -66,15 +66,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kXBox = 128;                   // activation rows per TMA box
 constexpr int kXBoxBytes = kXBox * kK * 2;  // 16 KiB
 
-template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_>
+template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_, bool kGateUp_ = false>
 struct TmemCfg {
     static constexpr int kTok = kTok_;        // tokens per item (MMA N)
     static constexpr int kMTw = kMTw_;        // 128-row weight tiles per item
     static constexpr int kAccBufs = kAccBufs_;  // accumulator buffers
+    // gate/up mode: the item's two weight tiles are gate rows n0.. and up rows
+    // n_out + n0.. of the same expert, and the epilogue writes silu(gate) * up
+    static constexpr bool kGateUp = kGateUp_;
     // a stage of the operand ring holds one slice's activation tile (shared memory)
     // and its decoded weights (tensor memory) under one full and one empty barrier
     static constexpr int S = kStages_, SR = kStagesRaw_;
     static constexpr int kWRows = kWM * kMTw;
+    static constexpr int kTileCols = kGateUp ? kWM : kWRows;  // output columns per item
     static constexpr int kWarpsPerSlice = 4 * kMTw;
     static constexpr int kGroups = kDecodeWarps / kWarpsPerSlice;
     // tensor memory: accumulator buffers, then the ring of decoded slices
@@ -91,6 +95,7 @@ struct TmemCfg {
     static constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
     static_assert(kTok == 128 || kTok == 256, "MMA N");
     static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
+    static_assert(!kGateUp || kMTw == 2, "gate/up items pair two weight tiles");
     static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
     static_assert(kAColBase + S * kAStageCols <= (int)kTmemCols, "tensor memory columns");
     static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -100,6 +105,8 @@ struct TmemCfg {
 using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
 // More tokens: 256 tokens per item against one weight tile.
 using CfgLarge = TmemCfg<256, 1, 1, 6, 8>;
+// Gate/up GEMM of the MoE layer with the activation function in the epilogue.
+using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true>;
 
 struct Item {
     int64_t row_begin, rows, m0;
@@ -108,12 +115,12 @@ struct Item {
 };
 
 // Item t: weight tile t % n_tiles (fastest), token slab, expert.
-__device__ __forceinline__ Item item_at(int64_t t, int n_tiles, int slabs, int tok, int wrows,
+__device__ __forceinline__ Item item_at(int64_t t, int n_tiles, int slabs, int tok, int cols,
                                         const int64_t *__restrict__ offsets, int64_t max_rows,
                                         int64_t total_rows) {
     Item it;
     const int64_t rest = t / n_tiles;
-    it.n0 = (int)(t - rest * n_tiles) * wrows;
+    it.n0 = (int)(t - rest * n_tiles) * cols;
     it.expert = (int)(rest / slabs);
     it.m0 = (rest - (int64_t)it.expert * slabs) * tok;
     it.row_begin = __ldg(offsets + it.expert);
@@ -124,14 +131,22 @@ __device__ __forceinline__ Item item_at(int64_t t, int n_tiles, int slabs, int t
     return it;
 }
 
+// silu(g) * u of two fp32 accumulator words: g / (1 + e^-g) * u in fp32 (e^-g
+// from expf; a gate below about -88 gives e^-g = inf and a signed zero).
+__device__ __forceinline__ float silu_mul(uint32_t gate_bits, uint32_t up_bits) {
+    const float g = __uint_as_float(gate_bits);
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), __uint_as_float(up_bits));
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
 mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_w,
                         const int64_t *__restrict__ expert_offsets,
                         const uint8_t *__restrict__ w_scales, int32_t experts, int64_t max_rows,
-                        int64_t total_rows, int32_t n, int32_t k, uint16_t *__restrict__ out,
-                        int32_t *__restrict__ status) {
+                        int64_t total_rows, int32_t n_rows, int32_t n_out, int32_t k,
+                        uint16_t *__restrict__ out, int32_t *__restrict__ status) {
+    // n_rows: weight rows per expert (2 n_out in gate/up mode); n_out: output columns
     constexpr int kTok = C::kTok, kMTw = C::kMTw, S = C::S, SR = C::SR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -151,13 +166,13 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int n_tiles = (n + C::kWRows - 1) / C::kWRows;
+    const int n_tiles = (n_out + C::kTileCols - 1) / C::kTileCols;
     const int slabs = (int)((max_rows + kTok - 1) / kTok);
     const int64_t n_items = (int64_t)experts * slabs * n_tiles;
     const int nk = (k + kK - 1) / kK;
     const int scale_pitch = k / 32;
     auto item = [&](int64_t t) {
-        return item_at(t, n_tiles, slabs, kTok, C::kWRows, expert_offsets, max_rows, total_rows);
+        return item_at(t, n_tiles, slabs, kTok, C::kTileCols, expert_offsets, max_rows, total_rows);
     };
     // tokens of an item that are computed: a slab whose live rows fit in 128 takes
     // N = 128 MMAs and one activation box per slice
@@ -215,8 +230,11 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
             const Item it = item(t);
             if (!it.live) continue;
-            const bool row_ok = it.n0 + r < n;
-            const uint8_t *srow = w_scales + ((int64_t)it.expert * n + it.n0 + r) * scale_pitch;
+            // the weight row this thread decodes (within the expert) and whether it exists
+            const int i_tile = r - mt * kWM;
+            const int wr = C::kGateUp ? mt * n_out + it.n0 + i_tile : it.n0 + r;
+            const bool row_ok = C::kGateUp ? it.n0 + i_tile < n_out : wr < n_out;
+            const uint8_t *srow = w_scales + ((int64_t)it.expert * n_rows + wr) * scale_pitch;
             // the row's two E8M0 bytes of slice kt; those of the group's next slice
             // are loaded one slice ahead, so their latency hides behind a slice
             auto scale_at = [&](int kt, int h) {
@@ -289,15 +307,44 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const int n_tok = (int)(tok_rows < kTok ? tok_rows : kTok);
             const int c_end = (n_tok + 31) & ~31;
             const bool odd = lane & 1;
+            if constexpr (C::kGateUp) {
+                // column c of the output: gate in accumulator tile 0, up in tile 1
+                const int col = it.n0 + quarter * 32 + (lane & ~1);
+                const bool col_ok = col < n_out;
+                uint16_t *optr = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n_out + col;
+                const int64_t step2 = 2 * (int64_t)n_out;
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * C::kAccCols);
+#pragma unroll 1
+                for (int c0 = 0; c0 < c_end; c0 += 16) {
+                    uint32_t gate[16], up[16];
+                    tmem_ld16(taddr + (uint32_t)c0, gate);
+                    tmem_ld16(taddr + (uint32_t)(kTok + c0), up);
+                    if (c0 + 16 >= c_end) {  // the buffer is read out
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty(b));
+                    }
+                    const int lim = n_tok - c0 - (odd ? 1 : 0);
+#pragma unroll
+                    for (int q = 0; q < 16; q += 2) {
+                        const uint32_t mine = pack_bf16x2_rn(silu_mul(gate[q], up[q]),
+                                                             silu_mul(gate[q + 1], up[q + 1]));
+                        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+                        const uint32_t word = odd ? prmt(other, mine, 0x7632u) : prmt(mine, other, 0x5410u);
+                        if (col_ok && q < lim) *reinterpret_cast<uint32_t *>(optr) = word;
+                        optr += step2;
+                    }
+                }
+            } else
 #pragma unroll 1
             for (int mt = 0; mt < kMTw; ++mt) {
                 // lanes 2i and 2i+1 hold output columns c and c+1 (c even); after an
                 // exchange the even lane stores both columns of token t and the odd
                 // lane both columns of token t + 1
                 const int col = it.n0 + mt * kWM + quarter * 32 + (lane & ~1);
-                const bool col_ok = col < n;
-                uint16_t *optr = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n + col;
-                const int64_t step2 = 2 * (int64_t)n;
+                const bool col_ok = col < n_out;
+                uint16_t *optr = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n_out + col;
+                const int64_t step2 = 2 * (int64_t)n_out;
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
                                        (uint32_t)(b * C::kAccCols + mt * kTok);
 #pragma unroll 1
@@ -355,7 +402,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
             const Item it = item(t);
             if (!it.live) continue;
-            const int w_row = it.expert * n + it.n0;
+            const int w_row = it.expert * n_rows + it.n0;  // gate rows in gate/up mode
             for (int kt = 0; kt < nk; ++kt, ++g) {
                 if (g >= (uint32_t)SR && !mbar_wait_bounded(empty_raw(s), ph ^ 1u)) *abort_flag = 1;
                 if (*abort_flag) {
@@ -364,6 +411,9 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 }
                 mbar_arrive_expect_tx(full_raw(s), (uint32_t)C::kRawBytes);
                 tma_load_2d(raw_ring + s * C::kRawBytes, &map_w, kt * (kK / 2), w_row, full_raw(s));
+                if (C::kGateUp)  // the matching up rows fill the second half of the stage
+                    tma_load_2d(raw_ring + s * C::kRawBytes + kWM * (kK / 2), &map_w, kt * (kK / 2),
+                                w_row + n_out, full_raw(s));
                 if (++s == SR) { s = 0; ph ^= 1u; }
             }
         }
@@ -443,9 +493,9 @@ int sm_count() {
 
 // Tensor maps of the activations [total_rows, k] bf16 (64 x 128 boxes, 128-byte
 // swizzle; rows past total_rows and columns past k read as zero) and of the packed
-// weights [experts * n, k / 2] uint8 (32-byte x wrows boxes, no swizzle).
+// weights [experts * n_rows, k / 2] uint8 (32-byte x box_rows boxes, no swizzle).
 cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_t *w_packed,
-                             int64_t experts, int64_t n, int64_t k, int wrows, CUtensorMap *map_x,
+                             int64_t experts, int64_t n_rows, int64_t k, int box_rows, CUtensorMap *map_x,
                              CUtensorMap *map_w) {
     EncodeTiled encode = tensor_map_encoder();
     if (encode == nullptr) return cudaErrorNotSupported;
@@ -461,9 +511,9 @@ cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_
             return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)(experts * n)};
+        const cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)(experts * n_rows)};
         const cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
-        const cuuint32_t box[2] = {kK / 2, (cuuint32_t)wrows};
+        const cuuint32_t box[2] = {kK / 2, (cuuint32_t)box_rows};
         if (encode(map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_packed), dims,
                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -476,8 +526,8 @@ cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_
 template <class C>
 cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_t experts,
                         int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
-                        const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
-                        int32_t *status, cudaStream_t stream) {
+                        const uint8_t *w_scales, int64_t n_rows, int64_t n_out, int64_t k,
+                        uint16_t *out, int32_t *status, cudaStream_t stream) {
     static thread_local int configured_device = -1;
     int device = 0;
     cudaError_t err = cudaGetDevice(&device);
@@ -489,16 +539,17 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
         configured_device = device;
     }
     CUtensorMap map_x, map_w;
-    err = tmem_tensor_maps(a, total_rows, w_packed, experts, n, k, C::kWRows, &map_x, &map_w);
+    err = tmem_tensor_maps(a, total_rows, w_packed, experts, n_rows, k,
+                           C::kGateUp ? kWM : C::kWRows, &map_x, &map_w);
     if (err != cudaSuccess) return err;
     const int64_t items = experts * ((max_rows + C::kTok - 1) / C::kTok) *
-                          ((n + C::kWRows - 1) / C::kWRows);
+                          ((n_out + C::kTileCols - 1) / C::kTileCols);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(items < sms ? items : sms);
     mx_moe_gemm_kernel<C><<<grid, kThreads, C::kSmemBytes, stream>>>(
         map_x, map_w, expert_offsets, w_scales, (int32_t)experts, max_rows, total_rows,
-        (int32_t)n, (int32_t)k, out, status);
+        (int32_t)n_rows, (int32_t)n_out, (int32_t)k, out, status);
     return cudaGetLastError();
 }
 
@@ -510,9 +561,17 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
                                int32_t *status, cudaStream_t stream) {
     if (max_rows > 128)
         return launch_tmem<CfgLarge>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
-                                     w_scales, n, k, out, status, stream);
+                                     w_scales, n, n, k, out, status, stream);
     return launch_tmem<CfgSmall>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
-                                 w_scales, n, k, out, status, stream);
+                                 w_scales, n, n, k, out, status, stream);
+}
+
+cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offsets, int64_t experts,
+                                  int64_t max_rows, int64_t total_rows, const uint8_t *w1_packed,
+                                  const uint8_t *w1_scales, int64_t n, int64_t k, uint16_t *act,
+                                  int32_t *status, cudaStream_t stream) {
+    return launch_tmem<CfgGateUp>(x, expert_offsets, experts, max_rows, total_rows, w1_packed,
+                                  w1_scales, 2 * n, n, k, act, status, stream);
 }
 
 }  // namespace fp4mx

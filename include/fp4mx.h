@@ -219,6 +219,62 @@ fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *expert_offsets
                            uint16_t *out_bf16, int32_t *status, fp4_stream_t stream);
 
 /*
+ * fp4_mx_moe_forward -- the MoE layer with MXFP4 experts: routing, gate/up GEMM,
+ * silu(gate) * up, down GEMM and the top-k weighted sum, all on the device.
+ *
+ * The layer the pages' unpack feeds: "vllm-project/vllm pull 51583" (prhub
+ * digest), the CPU test that runs ops.fused_experts_cpu with MXFP4 experts and
+ * the zero-code test whose comment notes that silu(0) * 0 = 0 collapses the
+ * layer to exact zeros. For token m and each slot j < topk with expert
+ * e = topk_ids[m][j] and weight w = topk_weights[m][j]:
+ *     h   = a[m] @ W1_e^T               W1_e [2n, k]: rows 0..n-1 gate, n..2n-1 up
+ *     act = bf16(silu(h[:n]) * h[n:])   silu(x) = x / (1 + exp(-x)), fp32
+ *     y   = bf16(act @ W2_e^T)          W2_e [k, n]
+ *     out[m] = bf16(sum_j w * y)        fp32, slots in order j = 0, 1, ...
+ * where W1_e and W2_e are what fp4_mx_unpack gives for the expert's packed rows,
+ * and the GEMMs accumulate in fp32 on the tensor core (order unspecified).
+ *
+ *   a_bf16               device, uint16[tokens * k] bf16 bits, row-major; 16-byte aligned
+ *   topk_ids             device, int32[tokens * topk]; an id outside [0, experts)
+ *                        contributes nothing and status is set to FP4_ERR_INDEX
+ *   topk_weights         device, fp32[tokens * topk]
+ *   tokens, topk         tokens >= 0 (0: nothing is launched), 1 <= topk <= 1024,
+ *                        tokens * topk < 2^31
+ *   experts              1 .. 65535
+ *   max_rows_per_expert  capacity of one expert (values above tokens * topk are
+ *                        treated as tokens * topk); the slots of an expert that
+ *                        holds more rows contribute nothing and status is set to
+ *                        FP4_ERR_SHAPE. When no token repeats an expert among its
+ *                        slots, tokens is always enough.
+ *   w1_packed            device, uint8[experts * 2n * k / 2]; 16-byte aligned
+ *   w1_scales_e8m0       device, uint8[experts * 2n * k / 32]
+ *   w2_packed            device, uint8[experts * k * n / 2]; 16-byte aligned
+ *   w2_scales_e8m0       device, uint8[experts * k * n / 32]
+ *   n, k                 intermediate and hidden sizes: multiples of 32, 32 .. 2^20
+ *   workspace            device scratch of workspace_bytes >= fp4_mx_moe_workspace_bytes(),
+ *                        256-byte aligned; owned by the caller, overwritten by the call,
+ *                        not read afterwards
+ *   out_bf16             device, uint16[tokens * k], row-major; 16-byte aligned
+ *   status               device int32, required; FP4_ERR_INDEX / FP4_ERR_SHAPE as
+ *                        above or FP4_ERR_TIMEOUT from a GEMM; never cleared
+ *   stream               CUDA stream every kernel is enqueued on
+ * Returns FP4_ERR_SHAPE for bad sizes or a short workspace, FP4_ERR_ALIAS when the
+ * output or the workspace overlaps an input or each other.
+ */
+fp4_status fp4_mx_moe_forward(const uint16_t *a_bf16, const int32_t *topk_ids,
+                              const float *topk_weights, int64_t tokens, int64_t topk,
+                              int64_t experts, int64_t max_rows_per_expert,
+                              const uint8_t *w1_packed, const uint8_t *w1_scales_e8m0,
+                              const uint8_t *w2_packed, const uint8_t *w2_scales_e8m0, int64_t n,
+                              int64_t k, void *workspace, int64_t workspace_bytes,
+                              uint16_t *out_bf16, int32_t *status, fp4_stream_t stream);
+
+/* Bytes of workspace fp4_mx_moe_forward needs for these sizes (about
+ * tokens * topk * (4k + 2n) bytes), or -1 when the sizes are invalid. */
+int64_t fp4_mx_moe_workspace_bytes(int64_t tokens, int64_t topk, int64_t experts, int64_t n,
+                                   int64_t k);
+
+/*
  * fp4_nv_dequant -- dequantise a whole NVFP4 table (every row, in order).
  *
  * The dense counterpart of fp4_nv_embedding_gather: out[r][c] is what the
@@ -250,7 +306,8 @@ const char *fp4_last_error(void);
 
 /* Version of this ABI (major * 100 + minor): 101 adds fp4_nv_dequant, 102 adds
  * fp4_mx_quantize and FP4_ERR_ALIGN, 103 adds fp4_mx_moe_gemm and FP4_ERR_TIMEOUT,
- * 104 adds fp4_mx_unpack_pages. */
+ * 104 adds fp4_mx_unpack_pages, 105 adds fp4_mx_moe_forward and
+ * fp4_mx_moe_workspace_bytes. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

@@ -259,24 +259,39 @@ class Oracle:
             absdot[r0:r1] = np.abs(a[r0:r1]) @ np.abs(w).T
         return out, absdot
 
+    @staticmethod
+    def bf16_round(x) -> np.ndarray:
+        """Round float64 values to the nearest bf16 value (ties to even), as float64:
+        8 significant bits, spacing 2^-133 below the smallest normal 2^-126."""
+        x = np.asarray(x, dtype=np.float64)
+        out = x.copy()
+        nz = (x != 0) & np.isfinite(x)
+        _, e = np.frexp(x[nz])  # x = f * 2^e, 0.5 <= |f| < 1
+        ulp = np.ldexp(1.0, np.maximum(e, -125) - 8)
+        out[nz] = np.rint(x[nz] / ulp) * ulp
+        return out
+
     def mx_moe_forward(self, a_bits, topk_ids, topk_weights, w1_packed, w1_scales, w2_packed,
                        w2_scales, threads: int = 1) -> dict:
         """The MoE layer the unpack feeds ("vllm-project/vllm pull 51583": the test that
         runs ops.fused_experts_cpu with MXFP4 experts, and the zero-code test whose
-        comment says silu(0) * 0 = 0 collapses the whole layer to exact zeros). For
-        token m and each of its top-k slots j, with expert e = topk_ids[m, j] and
-        weight w = topk_weights[m, j]:
-            h   = a[m] @ W1_e^T            W1_e [2N, K] unpacked (gate rows, then up rows)
-            act = silu(h[:N]) * h[N:]      silu(x) = x / (1 + exp(-x))
-            y   = act @ W2_e^T             W2_e [K, N] unpacked
-            out[m] += w * y
-        all in float64 with no intermediate rounding (bf16 x bf16 products are exact,
-        the sums far more precise than the fp32 work they are compared with). A slot
-        whose expert id is outside [0, E) contributes nothing and is counted.
+        comment says silu(0) * 0 = 0 collapses the whole layer). For token m and each
+        of its top-k slots j, with expert e = topk_ids[m, j] and weight w =
+        topk_weights[m, j]:
+            h   = a[m] @ W1_e^T                  W1_e [2N, K] unpacked (gate rows, then up)
+            act = bf16(silu(h[:N]) * h[N:])      silu(x) = x / (1 + exp(-x))
+            y   = bf16(act @ W2_e^T)             W2_e [K, N] unpacked
+            out[m] = bf16(sum_j w * y)
+        where each bf16() rounds the exact value (nearest, ties to even) -- the places
+        the layer stores bf16 -- and everything else is float64 (bf16 x bf16 products
+        are exact, the sums far more precise than the fp32 work they are compared
+        with). A slot whose expert id is outside [0, E) contributes nothing and is
+        counted.
 
-        Returns a dict: out [M, K]; the per-slot g, u, act [M, topk, N] and y
-        [M, topk, K]; sg, su [M, topk, N] = sums of |a||w1| behind g and u; the
-        unpacked weights w1 [E, 2N, K], w2 [E, K, N] (float64); bad (count)."""
+        Returns a dict: out [M, K] (rounded) and out_exact (before its rounding); per
+        slot g, u, act_exact, act [M, topk, N] and y_exact, y [M, topk, K]; sg, su
+        [M, topk, N] = sums of |a||w1| behind g and u; the unpacked weights w1 [E, 2N,
+        K], w2 [E, K, N] (float64); bad (count)."""
         a = self.bf16_to_f64(a_bits)
         ids = np.asarray(topk_ids, dtype=np.int64)
         wts = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
@@ -294,9 +309,11 @@ class Oracle:
         u = np.zeros((m_tok, topk, n))
         sg = np.zeros((m_tok, topk, n))
         su = np.zeros((m_tok, topk, n))
+        act_exact = np.zeros((m_tok, topk, n))
         act = np.zeros((m_tok, topk, n))
+        y_exact = np.zeros((m_tok, topk, k))
         y = np.zeros((m_tok, topk, k))
-        out = np.zeros((m_tok, k))
+        out_exact = np.zeros((m_tok, k))
         bad = int(np.count_nonzero((ids < 0) | (ids >= experts)))
         for e in range(experts):
             ms, js = np.nonzero(ids == e)
@@ -309,12 +326,17 @@ class Oracle:
             sg[ms, js], su[ms, js] = habs[:, :n], habs[:, n:]
             with np.errstate(over="ignore"):
                 act_e = h[:, :n] / (1.0 + np.exp(-h[:, :n])) * h[:, n:]
-            act[ms, js] = act_e
-            y_e = act_e @ w2[e].T
-            y[ms, js] = y_e
-            np.add.at(out, ms, wts[ms, js][:, None] * y_e)
-        return {"out": out, "g": g, "u": u, "sg": sg, "su": su, "act": act, "y": y,
-                "w1": w1, "w2": w2, "bad": bad}
+            act_exact[ms, js] = act_e
+            act_r = self.bf16_round(act_e)
+            act[ms, js] = act_r
+            y_e = act_r @ w2[e].T
+            y_exact[ms, js] = y_e
+            y_r = self.bf16_round(y_e)
+            y[ms, js] = y_r
+            np.add.at(out_exact, ms, wts[ms, js][:, None] * y_r)
+        return {"out": self.bf16_round(out_exact), "out_exact": out_exact, "g": g, "u": u,
+                "sg": sg, "su": su, "act_exact": act_exact, "act": act, "y_exact": y_exact,
+                "y": y, "w1": w1, "w2": w2, "bad": bad}
 
     # -- NVFP4 ----------------------------------------------------------------
     def nv_embedding_gather(self, ids, weight, scales, global_scale, group_size: int = 16,

@@ -474,9 +474,32 @@ def pin_moe_forward_zero_codes_collapse(o):
             assert np.all(r["out"] == 0.0), (zero_byte, e8m0)
 
 
+def _bf16_round_scalar(x: float) -> float:
+    """Nearest bf16 value (ties to even) of a Python float, by frexp and round()."""
+    import math
+    if x == 0.0 or not math.isfinite(x):
+        return x
+    _, e = math.frexp(x)
+    ulp = 2.0 ** (max(e, -125) - 8)
+    return round(x / ulp) * ulp
+
+
+def pin_bf16_round_matches_torch(o):
+    """The oracle's float64 -> bf16 rounding equals torch's float32 -> bfloat16
+    conversion (a library routine, ties to even) on values that are exact in
+    float32, including ties, subnormals and both signs."""
+    rng = np.random.default_rng(99)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        (rng.integers(-2 ** 15, 2 ** 15, 4000) * 2.0 + 1) * 2.0 ** -16,  # ties
+                        rng.standard_normal(2000) * 2.0 ** -128]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(o.bf16_round(x.astype(np.float64)), want)
+
+
 def pin_moe_forward_brute_force(o):
     """A tiny layer against plain scalar loops over the decoded codes (gate rows
-    first, silu(x) = x / (1 + e^-x), both GEMMs, the weighted top-k sum)."""
+    first, silu(x) = x / (1 + e^-x), both GEMMs, bf16 roundings of act, y and out,
+    the weighted top-k sum)."""
     import math
     rng = np.random.default_rng(93)
     m_tok, k, n, experts, topk = 3, 32, 32, 3, 2
@@ -500,19 +523,19 @@ def pin_moe_forward_brute_force(o):
         return (-1.0 if c & 8 else 1.0) * mags[c & 7] * 2.0 ** (int(e8m0) - 127)
 
     for m in range(m_tok):
-        expect = [0.0] * k
+        total = [0.0] * k
         for j in range(topk):
             e = int(ids[m, j])
             hid = []
             for i in range(n):
                 gate = sum(a_vals[m, kk] * val(c1[e, i, kk], s1[e, i, kk // 32]) for kk in range(k))
                 up = sum(a_vals[m, kk] * val(c1[e, n + i, kk], s1[e, n + i, kk // 32]) for kk in range(k))
-                hid.append(gate / (1.0 + math.exp(-gate)) * up)
+                hid.append(_bf16_round_scalar(gate / (1.0 + math.exp(-gate)) * up))
             for c in range(k):
-                yc = sum(hid[i] * val(c2[e, c, i], s2[e, c, i // 32]) for i in range(n))
-                expect[c] += float(wts[m, j]) * yc
-        got = r["out"][m]
-        assert np.allclose(got, expect, rtol=1e-12, atol=1e-12 * max(1.0, max(map(abs, expect)))), m
+                yc = _bf16_round_scalar(sum(hid[i] * val(c2[e, c, i], s2[e, c, i // 32]) for i in range(n)))
+                total[c] += float(wts[m, j]) * yc
+        expect = [_bf16_round_scalar(t) for t in total]
+        assert np.array_equal(r["out"][m], expect), m
 
 
 def pin_moe_forward_routing_invariants(o):

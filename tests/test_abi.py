@@ -56,7 +56,7 @@ def test_status_strings(lib):
     for code in range(1, 11):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 104
+    assert lib.fp4_abi_version() == 105
 
 
 def test_mx_host_validation(lib):
@@ -163,3 +163,40 @@ def test_binding_refuses_cpu_tensors():
                                     torch.zeros(4, 8, dtype=torch.uint8),
                                     torch.zeros(4, 1, dtype=torch.uint8),
                                     torch.ones(1, dtype=torch.float32))
+
+
+def test_moe_forward_host_validation(lib):
+    """Sizes, pointers, alignment, workspace size and aliasing are checked on the host
+    before any CUDA call (fake device addresses: nothing is dereferenced)."""
+    ws = lib.fp4_mx_moe_workspace_bytes
+    assert ws(16, 2, 4, 64, 64) > 16 * 2 * (4 * 64 + 2 * 64)
+    assert ws(16, 2, 4, 63, 64) == -1 and ws(16, 2, 4, 64, 48) == -1      # n, k % 32
+    assert ws(16, 0, 4, 64, 64) == -1 and ws(16, 2, 0, 64, 64) == -1      # topk, experts
+    assert ws(2 ** 30, 4, 4, 64, 64) == -1                                 # slots >= 2^31
+    f = lib.fp4_mx_moe_forward
+    base = 1 << 40
+    tokens, topk, experts, n, k = 16, 2, 4, 64, 64
+    need = ws(tokens, topk, experts, n, k)
+    a, ids, wts = base, base + (1 << 20), base + (2 << 20)
+    w1, s1, w2, s2 = base + (3 << 20), base + (4 << 20), base + (5 << 20), base + (6 << 20)
+    work, out, st = base + (8 << 20), base + (16 << 20), base + (17 << 20)
+
+    def call(**kw):
+        args = dict(a=a, ids=ids, wts=wts, tokens=tokens, topk=topk, experts=experts, cap=tokens,
+                    w1=w1, s1=s1, w2=w2, s2=s2, n=n, k=k, work=work, work_bytes=need, out=out, st=st)
+        args.update(kw)
+        return f(args["a"], args["ids"], args["wts"], args["tokens"], args["topk"], args["experts"],
+                 args["cap"], args["w1"], args["s1"], args["w2"], args["s2"], args["n"], args["k"],
+                 args["work"], args["work_bytes"], args["out"], args["st"], None)
+
+    assert call(n=48) == fp4.Status.ERR_SHAPE
+    assert call(cap=-1) == fp4.Status.ERR_SHAPE
+    assert call(tokens=0, a=None, ids=None) == fp4.Status.OK               # nothing launched
+    assert call(st=None) == fp4.Status.ERR_NULL_PTR
+    assert call(work=None) == fp4.Status.ERR_NULL_PTR
+    assert call(a=a + 2) == fp4.Status.ERR_ALIGN
+    assert call(work=work + 16) == fp4.Status.ERR_ALIGN                    # 256-byte workspace
+    assert call(work_bytes=need - 1) == fp4.Status.ERR_SHAPE
+    assert call(out=a) == fp4.Status.ERR_ALIAS
+    assert call(work=w1 - 256) == fp4.Status.ERR_ALIAS                     # workspace over w1
+    assert call(out=work + 256) == fp4.Status.ERR_ALIAS

@@ -1,0 +1,227 @@
+"""GPU parity of the MoE layer (routing, gate/up GEMM with silu(gate) * up, down GEMM,
+top-k weighted sum) against the float64 oracle, which rounds act, y and out to bf16
+exactly where the layer stores bf16.
+
+The bound follows the kernels' arithmetic stage by stage. Before each bf16 store
+the GPU value differs from the oracle's exact value by at most `pre` (below);
+rounding then gives the same bf16 value unless a rounding midpoint lies within
+`pre` of the exact value, in which case the two can differ by `pre` plus one bf16
+spacing:
+  act  pre = 1.1 |u| dg + (|silu(g)| + 1.1 dg) du + 2^-20 |act|, with
+       dg = (1 + 2^-8) k 2^-23 sum|a w1| the fp32 accumulation bound of the gate
+       (du likewise) and 2^-20 for fp32 silu (expf, add, divide, multiply);
+       dg = du = 0 when the inputs make the gate/up sums exact in fp32 (dyadic
+       activations and weight scales: every partial sum fits in 24 bits)
+  y    pre = dact @ |W2|^T + (1 + 2^-8) n 2^-23 (|act| + dact) @ |W2|^T
+  out  pre = sum_j |w_j| dy_j + topk 2^-23 sum_j |w_j| (|y_j| + dy_j).
+With dyadic inputs the bound is about the down GEMM's own accumulation bound, so
+a swapped gate/up, a wrong activation, a dropped weight or a slot routed to the
+wrong expert is far outside it. With normal activations the gate/up bound, taken
+worst case through the down GEMM, is loose; those tests add a median-error check.
+"""
+import numpy as np
+import pytest
+
+import block_scaled_fp4_mx_gb300 as fp4
+from block_scaled_fp4_mx_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+EPS = 2.0 ** -23
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def bf16_spacing(x):
+    """Spacing of bf16 values at |x| (2^-133 below the smallest normal)."""
+    _, e = np.frexp(np.abs(x))
+    return np.ldexp(1.0, np.maximum(e, -125) - 8)
+
+
+def after_rounding(exact, pre):
+    """Bound on |bf16(gpu) - bf16(exact)| given |gpu - exact| <= pre: zero unless a
+    rounding midpoint lies within pre of exact (checked with half the spacing, so
+    the spacing change at a power of two is covered)."""
+    sp = bf16_spacing(exact)
+    t = np.abs(exact) / sp
+    dist_mid = np.abs(t - np.floor(t) - 0.5) * sp * 0.5
+    return np.where(pre < dist_mid, 0.0, pre + bf16_spacing(np.abs(exact) + pre))
+
+
+def forward_bound(r, ids, wts, k, n, topk, exact_gemm1):
+    g, u = r["g"], r["u"]
+    if exact_gemm1:
+        d1 = np.zeros_like(g)
+    else:
+        dg = (1 + 2.0 ** -8) * k * EPS * r["sg"]
+        du = (1 + 2.0 ** -8) * k * EPS * r["su"]
+        with np.errstate(over="ignore"):
+            silu = g / (1.0 + np.exp(-g))
+        d1 = 1.1 * np.abs(u) * dg + (np.abs(silu) + 1.1 * dg) * du
+    act_pre = d1 + 2.0 ** -20 * (np.abs(r["act_exact"]) + d1)
+    dact = after_rounding(r["act_exact"], act_pre)
+    experts = r["w2"].shape[0]
+    dy = np.zeros_like(r["y"])
+    for e in range(experts):
+        ms, js = np.nonzero(ids == e)
+        if ms.size == 0:
+            continue
+        w2abs = np.abs(r["w2"][e]).T  # [n, k]
+        pre = dact[ms, js] @ w2abs + (1 + 2.0 ** -8) * n * EPS * ((np.abs(r["act"][ms, js]) + dact[ms, js]) @ w2abs)
+        dy[ms, js] = after_rounding(r["y_exact"][ms, js], pre)
+    valid = ((ids >= 0) & (ids < experts)).astype(np.float64)
+    wabs = np.abs(wts.astype(np.float64)) * valid
+    pre = np.einsum("mj,mjc->mc", wabs, dy + topk * EPS * (np.abs(r["y"]) + dy))
+    return after_rounding(r["out_exact"], pre)
+
+
+def make_layer(tokens, k, n, experts, topk, seed, dyadic=True):
+    """Random layer. dyadic: activations in {-1, -7/8, ..., 1} and gate/up scales
+    2^-2..2^1, so that every gate/up partial sum is exact in fp32."""
+    rng = np.random.default_rng(seed)
+    if dyadic:
+        a_vals = rng.integers(-8, 9, size=(tokens, k)) / 8.0
+        a_bits = (a_vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        e1 = (125, 128)
+    else:
+        a_bits = inputs.bf16_normal_bits(rng, tokens * k).reshape(tokens, k)
+        e1 = (119, 125)
+    ids = np.stack([rng.permutation(experts)[:topk] for _ in range(tokens)]).astype(np.int32)
+    wts = rng.random((tokens, topk)).astype(np.float32)
+    wts /= wts.sum(axis=1, keepdims=True)
+    w1 = inputs.mx_random(experts * 2 * n, k, seed + 1, e_lo=e1[0], e_hi=e1[1], zero_fraction=True)
+    w2 = inputs.mx_random(experts * k, n, seed + 2, e_lo=119, e_hi=125, zero_fraction=True)
+    return dict(a_bits=a_bits, ids=ids, wts=wts, dyadic=dyadic,
+                w1p=w1.packed.reshape(experts, 2 * n, k // 2), w1s=w1.scales.reshape(experts, 2 * n, k // 32),
+                w2p=w2.packed.reshape(experts, k, n // 2), w2s=w2.scales.reshape(experts, k, n // 32))
+
+
+def run_gpu(L, max_rows=None):
+    t = {key: torch.from_numpy(v).to(DEV) for key, v in L.items()
+         if isinstance(v, np.ndarray) and key != "a_bits"}
+    a = torch.from_numpy(L["a_bits"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    out, status = fp4.fp4_mx_moe_forward(a, t["ids"], t["wts"], t["w1p"], t["w1s"], t["w2p"], t["w2s"],
+                                         max_rows_per_expert=max_rows)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), int(status.item())
+
+
+def check(oracle_impl, L, max_rows=None, expect_status=0, oracle_ids=None):
+    got, status = run_gpu(L, max_rows)
+    assert status == expect_status, f"device status {status}"
+    ids = L["ids"] if oracle_ids is None else oracle_ids
+    k, n = L["a_bits"].shape[1], L["w2p"].shape[2] * 2
+    r = oracle_impl.mx_moe_forward(L["a_bits"], ids, L["wts"], L["w1p"], L["w1s"], L["w2p"], L["w2s"],
+                                   threads=oracle_impl.max_threads())
+    tol = forward_bound(r, ids, L["wts"], k, n, ids.shape[1], exact_gemm1=L["dyadic"])
+    err = np.abs(got - r["out"])
+    bad = err > tol
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{int(bad.sum())} of {bad.size} outside the bound; first {i}: gpu {got[i]} "
+                             f"oracle {r['out'][i]} tol {tol[i]}")
+    if not L["dyadic"]:  # the worst-case bound is loose here: typical error must still be small
+        nz = np.abs(r["out"]) > 0
+        assert np.median(err[nz] / np.abs(r["out"][nz])) <= 2.0 ** -6
+    return got, r
+
+
+def test_pages_zero_code_layer_is_exactly_zero():
+    """The pages' zero-code MoE test (N = K = 64, E = 2, M = 4, every token on expert
+    0): gate/up weights of one zero code at any E8M0 give exact zeros."""
+    n, k, experts, tokens = 64, 64, 2, 4
+    rng = np.random.default_rng(7)
+    a = torch.from_numpy(inputs.bf16_normal_bits(rng, tokens * k).view(np.int16)).to(DEV)
+    a = a.view(torch.bfloat16).reshape(tokens, k)
+    w2 = inputs.mx_random(experts * k, n, seed=8, e_lo=118, e_hi=126)
+    w2p = torch.from_numpy(w2.packed.reshape(experts, k, n // 2)).to(DEV)
+    w2s = torch.from_numpy(w2.scales.reshape(experts, k, n // 32)).to(DEV)
+    ids = torch.zeros((tokens, 1), dtype=torch.int32, device=DEV)
+    wts = torch.ones((tokens, 1), dtype=torch.float32, device=DEV)
+    for zero_byte in (0x00, 0x88, 0x08, 0x80):
+        for e8m0 in (0, 1, 127, 200, 254, 255):
+            w1p = torch.full((experts, 2 * n, k // 2), zero_byte, dtype=torch.uint8, device=DEV)
+            w1s = torch.full((experts, 2 * n, k // 32), e8m0, dtype=torch.uint8, device=DEV)
+            out, status = fp4.fp4_mx_moe_forward(a, ids, wts, w1p, w1s, w2p, w2s)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            assert bool((out.float() == 0).all()), (zero_byte, e8m0)
+
+
+@pytest.mark.parametrize("tokens,k,n,experts,topk", [(1, 32, 32, 1, 1), (40, 128, 96, 5, 2),
+                                                     (37, 64, 160, 3, 3), (130, 96, 64, 4, 1)])
+def test_small_layers(oracle_impl, tokens, k, n, experts, topk):
+    """Single token and expert; n and k that are not multiples of the 128-row tile;
+    experts holding more than 128 rows (two token slabs); topk 1 to 3."""
+    check(oracle_impl, make_layer(tokens, k, n, experts, topk, seed=tokens + k + n))
+
+
+def test_gpt_oss_like_layer(oracle_impl):
+    """Hidden 2880, intermediate 2880, 4 experts, top-4 of 64 tokens."""
+    check(oracle_impl, make_layer(64, 2880, 2880, 4, 4, seed=31))
+
+
+def test_gpt_oss_like_layer_normal_activations(oracle_impl):
+    """The same shapes with normal activations (loose worst-case bound plus the
+    median-error check)."""
+    check(oracle_impl, make_layer(64, 2880, 2880, 4, 4, seed=33, dyadic=False))
+
+
+def test_bad_expert_ids_contribute_nothing(oracle_impl):
+    L = make_layer(24, 64, 64, 3, 2, seed=41)
+    L["ids"][3, 0] = 3
+    L["ids"][9, 1] = -2
+    check(oracle_impl, L, expect_status=fp4.Status.ERR_INDEX)
+
+
+def test_repeated_expert_in_one_token(oracle_impl):
+    """A token may pick the same expert twice: two rows in that expert's segment."""
+    L = make_layer(16, 64, 64, 3, 2, seed=43)
+    L["ids"][:, 1] = L["ids"][:, 0]
+    check(oracle_impl, L, max_rows=32)
+
+
+def test_expert_over_capacity_is_dropped_and_flagged(oracle_impl):
+    """An expert holding more rows than max_rows_per_expert: its slots contribute
+    nothing and the status word says FP4_ERR_SHAPE."""
+    L = make_layer(20, 64, 64, 3, 1, seed=45)
+    L["ids"][:, 0] = np.where(np.arange(20) < 12, 1, np.arange(20) % 2 * 2).astype(np.int32)
+    oracle_ids = L["ids"].copy()
+    oracle_ids[oracle_ids == 1] = -1  # expert 1 holds 12 rows > capacity 10
+    check(oracle_impl, L, max_rows=10, expect_status=fp4.Status.ERR_SHAPE, oracle_ids=oracle_ids)
+
+
+def test_equals_gemm_composition():
+    """With top-1 routing and weight 1 the layer is the gate/up GEMM, the activation
+    and the down GEMM of the standalone entry point, bit for bit in the down GEMM's
+    inputs: compare against fp4_mx_moe_gemm run on the layer's own activations."""
+    tokens, k, n, experts = 48, 128, 64, 2
+    L = make_layer(tokens, k, n, experts, 1, seed=47)
+    order = np.argsort(L["ids"][:, 0], kind="stable")
+    L["a_bits"], L["ids"] = L["a_bits"][order], L["ids"][order]
+    L["wts"] = np.ones_like(L["wts"])
+    got, status = run_gpu(L)
+    assert status == 0
+    counts = np.bincount(L["ids"][:, 0], minlength=experts)
+    offsets = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)).to(DEV)
+    a = torch.from_numpy(L["a_bits"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    h, st1 = fp4.fp4_mx_moe_gemm(a, offsets, torch.from_numpy(L["w1p"]).to(DEV),
+                                 torch.from_numpy(L["w1s"]).to(DEV), int(counts.max()))
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0
+    # the layer keeps gate/up in fp32; from the bf16 GEMM output the activation can
+    # differ by one bf16 step, so compare the layer with a tolerance of a few steps
+    hf = h.float()
+    act = (torch.nn.functional.silu(hf[:, :n]) * hf[:, n:]).to(torch.bfloat16)
+    y, st2 = fp4.fp4_mx_moe_gemm(act, offsets, torch.from_numpy(L["w2p"]).to(DEV),
+                                 torch.from_numpy(L["w2s"]).to(DEV), int(counts.max()))
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    ref = y.float().cpu().numpy().astype(np.float64)
+    scale = np.abs(ref).max()
+    assert np.abs(got - ref).max() <= 0.05 * scale

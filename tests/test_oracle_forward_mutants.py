@@ -20,12 +20,14 @@ MUTATIONS = [
      "act_e = h[:, :n] / (1.0 + np.exp(h[:, :n])) * h[:, n:]", "silu with the wrong sign"),
     ("act_e = h[:, :n] / (1.0 + np.exp(-h[:, :n])) * h[:, n:]",
      "act_e = np.maximum(h[:, :n], 0.0) * h[:, n:]", "relu instead of silu"),
-    ("np.add.at(out, ms, wts[ms, js][:, None] * y_e)", "np.add.at(out, ms, y_e)",
+    ("np.add.at(out_exact, ms, wts[ms, js][:, None] * y_r)", "np.add.at(out_exact, ms, y_r)",
      "top-k weights dropped"),
-    ("np.add.at(out, ms, wts[ms, js][:, None] * y_e)", "out[ms] = wts[ms, js][:, None] * y_e",
-     "slots of one token overwrite instead of add"),
+    ("np.add.at(out_exact, ms, wts[ms, js][:, None] * y_r)",
+     "out_exact[ms] = wts[ms, js][:, None] * y_r", "slots of one token overwrite instead of add"),
+    ("act_r = self.bf16_round(act_e)", "act_r = act_e", "activation not rounded to bf16"),
+    ("y_r = self.bf16_round(y_e)", "y_r = y_e", "down GEMM output not rounded to bf16"),
     ("h = rows @ w1[e].T", "h = rows @ w1[(e + 1) % experts].T", "another expert's gate/up weights"),
-    ("y_e = act_e @ w2[e].T", "y_e = act_e @ w2[(e + 1) % experts].T", "another expert's down weights"),
+    ("y_e = act_r @ w2[e].T", "y_e = act_r @ w2[(e + 1) % experts].T", "another expert's down weights"),
     (".reshape(k, n) for e in range(experts)]", ".reshape(n, k).T for e in range(experts)]",
      "down weights read transposed"),
     ("bad = int(np.count_nonzero((ids < 0) | (ids >= experts)))",
