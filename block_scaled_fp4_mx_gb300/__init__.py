@@ -31,7 +31,8 @@ from __future__ import annotations
 from ._lib import Status, last_error, library_path, load, status_string  # noqa: F401
 
 __all__ = ["fp4_mx_unpack", "fp4_mx_unpack_pages", "fp4_mx_quantize", "fp4_mx_moe_gemm",
-           "fp4_mx_moe_forward", "fp4_mx_moe_workspace_bytes",
+           "fp4_mx_moe_forward", "fp4_mx_moe_workspace_bytes", "fp4_mx_moe_forward_noalloc",
+           "fp4_mx_moe_static_scratch_bytes",
            "fp4_nv_embedding_gather",
            "fp4_nv_dequant",
            "fp4_status_string",
@@ -310,6 +311,56 @@ def fp4_mx_moe_forward(a, topk_ids, topk_weights, w1_packed, w1_scales, w2_packe
         _stream_handle(stream, a.device))
     if code != Status.OK:
         raise Fp4Error("fp4_mx_moe_forward", code)
+    return out, status
+
+
+def fp4_mx_moe_static_scratch_bytes() -> int:
+    """Bytes of the static device scratch fp4_mx_moe_forward_noalloc uses."""
+    return int(load().fp4_mx_moe_static_scratch_bytes())
+
+
+def fp4_mx_moe_forward_noalloc(a, topk_ids, topk_weights, w1_packed, w1_scales, w2_packed,
+                               w2_scales, max_rows_per_expert=None, out=None, status=None,
+                               stream=None):
+    """fp4_mx_moe_forward on the library's static device scratch: no workspace and
+    no allocation by the library (``out`` and ``status`` are allocated here when
+    not given). Layers that need more scratch than fp4_mx_moe_static_scratch_bytes()
+    raise Fp4Error (ERR_SHAPE). Calls must be ordered on one device. Returns
+    (out, status)."""
+    torch = _torch()
+    _check_cuda(a, "a", (torch.bfloat16, torch.int16, torch.uint16))
+    _check_cuda(topk_ids, "topk_ids", (torch.int32,))
+    _check_cuda(topk_weights, "topk_weights", (torch.float32,))
+    for t, name in ((w1_packed, "w1_packed"), (w1_scales, "w1_scales"), (w2_packed, "w2_packed"),
+                    (w2_scales, "w2_scales")):
+        _check_cuda(t, name, (torch.uint8,))
+    if a.dim() != 2 or topk_ids.dim() != 2 or w1_packed.dim() != 3 or w2_packed.dim() != 3:
+        raise ValueError("a [M, k], topk_ids [M, topk], w1_packed [E, 2n, k/2], w2_packed [E, k, n/2]")
+    tokens, k = a.shape
+    topk = topk_ids.shape[1]
+    experts, two_n, half_k = w1_packed.shape
+    n = two_n // 2
+    if (2 * half_k != k or two_n % 2 or topk_ids.shape[0] != tokens
+            or tuple(topk_weights.shape) != tuple(topk_ids.shape)
+            or tuple(w1_scales.shape) != (experts, two_n, k // 32)
+            or tuple(w2_packed.shape) != (experts, k, n // 2)
+            or tuple(w2_scales.shape) != (experts, k, n // 32)):
+        raise ValueError("inconsistent MoE layer shapes")
+    if out is None:
+        out = torch.empty((tokens, k), dtype=torch.bfloat16, device=a.device)
+    _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
+    if tuple(out.shape) != (tokens, k):
+        raise ValueError(f"out must have shape {(tokens, k)}")
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=a.device)
+    _check_cuda(status, "status", (torch.int32,))
+    max_rows = tokens if max_rows_per_expert is None else int(max_rows_per_expert)
+    code = load().fp4_mx_moe_forward_noalloc(
+        _ptr(a), _ptr(topk_ids), _ptr(topk_weights), tokens, topk, experts, max_rows,
+        _ptr(w1_packed), _ptr(w1_scales), _ptr(w2_packed), _ptr(w2_scales), n, k, _ptr(out),
+        _ptr(status), _stream_handle(stream, a.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_mx_moe_forward_noalloc", code)
     return out, status
 
 

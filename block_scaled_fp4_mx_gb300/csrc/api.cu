@@ -300,6 +300,35 @@ FP4_EXPORT fp4_status fp4_mx_moe_forward(const uint16_t *a_bf16, const int32_t *
     return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_mx_moe_forward launch");
 }
 
+FP4_EXPORT int64_t fp4_mx_moe_static_scratch_bytes(void) {
+    return (int64_t)fp4mx::moe_static_scratch_bytes();
+}
+
+FP4_EXPORT fp4_status fp4_mx_moe_forward_noalloc(
+    const uint16_t *a_bf16, const int32_t *topk_ids, const float *topk_weights, int64_t tokens,
+    int64_t topk, int64_t experts, int64_t max_rows_per_expert, const uint8_t *w1_packed,
+    const uint8_t *w1_scales_e8m0, const uint8_t *w2_packed, const uint8_t *w2_scales_e8m0,
+    int64_t n, int64_t k, uint16_t *out_bf16, int32_t *status, fp4_stream_t stream) {
+    clear_error();
+    if (!moe_shape_ok(tokens, topk, experts, n, k) || max_rows_per_expert < 0) return FP4_ERR_SHAPE;
+    if (tokens == 0) return FP4_OK;
+    const uint64_t need = fp4mx::moe_workspace_layout(tokens, topk, experts, n, k).total;
+    if (need > fp4mx::moe_static_scratch_bytes()) {  // size rejection: nothing is launched
+        std::snprintf(g_last_error, sizeof g_last_error,
+                      "the layer needs %llu bytes of scratch, the static area holds %llu",
+                      (unsigned long long)need,
+                      (unsigned long long)fp4mx::moe_static_scratch_bytes());
+        return FP4_ERR_SHAPE;
+    }
+    void *scratch = nullptr;
+    const cudaError_t err = fp4mx::moe_static_scratch(&scratch);
+    if (err != cudaSuccess) return cuda_failure(err, "static scratch address");
+    return fp4_mx_moe_forward(a_bf16, topk_ids, topk_weights, tokens, topk, experts,
+                              max_rows_per_expert, w1_packed, w1_scales_e8m0, w2_packed,
+                              w2_scales_e8m0, n, k, scratch, (int64_t)need, out_bf16, status,
+                              stream);
+}
+
 FP4_EXPORT fp4_status fp4_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,
                                           const uint8_t *packed_pool,
                                           const uint8_t *scales_pool_e8m0, int64_t pool_pages,
@@ -384,4 +413,4 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 105; }
+FP4_EXPORT int fp4_abi_version(void) { return 106; }

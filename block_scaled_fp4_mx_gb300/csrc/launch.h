@@ -57,6 +57,11 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
                                   const uint8_t *w2_scales, int64_t n, int64_t k, void *workspace,
                                   uint16_t *out, int32_t *status, cudaStream_t stream);
 
+// The MoE layer's static device scratch (fp4_mx_moe_forward_noalloc): its size,
+// and its address on the current device (looked up once per device).
+uint64_t moe_static_scratch_bytes();
+cudaError_t moe_static_scratch(void **address);
+
 // Paged MXFP4 dequant: num_pages (> 0) pages of page_elems (a positive multiple of
 // 32) codes gathered from a pool by id.
 cudaError_t launch_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,

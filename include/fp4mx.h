@@ -275,6 +275,31 @@ int64_t fp4_mx_moe_workspace_bytes(int64_t tokens, int64_t topk, int64_t experts
                                    int64_t k);
 
 /*
+ * fp4_mx_moe_forward_noalloc -- fp4_mx_moe_forward with the library's own static
+ * scratch instead of a caller workspace (no cudaMalloc anywhere on the path).
+ *
+ * Same arguments, semantics and errors as fp4_mx_moe_forward (above) minus the
+ * workspace. The scratch is a static __device__ array of
+ * fp4_mx_moe_static_scratch_bytes() bytes per device, in a module of its own
+ * that the driver loads (and zero-fills) the first time it is used; its address
+ * is looked up once per device. A layer whose workspace would exceed it is
+ * rejected with FP4_ERR_SHAPE before anything is launched (the reason is in
+ * fp4_last_error()). The area is shared by every call on a device: calls must be
+ * ordered (one stream, or events between streams); two overlapping calls would
+ * overwrite each other's scratch. Thread-safe on the host.
+ */
+fp4_status fp4_mx_moe_forward_noalloc(const uint16_t *a_bf16, const int32_t *topk_ids,
+                                      const float *topk_weights, int64_t tokens, int64_t topk,
+                                      int64_t experts, int64_t max_rows_per_expert,
+                                      const uint8_t *w1_packed, const uint8_t *w1_scales_e8m0,
+                                      const uint8_t *w2_packed, const uint8_t *w2_scales_e8m0,
+                                      int64_t n, int64_t k, uint16_t *out_bf16, int32_t *status,
+                                      fp4_stream_t stream);
+
+/* Bytes of the static scratch fp4_mx_moe_forward_noalloc uses (per device). */
+int64_t fp4_mx_moe_static_scratch_bytes(void);
+
+/*
  * fp4_nv_dequant -- dequantise a whole NVFP4 table (every row, in order).
  *
  * The dense counterpart of fp4_nv_embedding_gather: out[r][c] is what the
@@ -307,7 +332,8 @@ const char *fp4_last_error(void);
 /* Version of this ABI (major * 100 + minor): 101 adds fp4_nv_dequant, 102 adds
  * fp4_mx_quantize and FP4_ERR_ALIGN, 103 adds fp4_mx_moe_gemm and FP4_ERR_TIMEOUT,
  * 104 adds fp4_mx_unpack_pages, 105 adds fp4_mx_moe_forward and
- * fp4_mx_moe_workspace_bytes. */
+ * fp4_mx_moe_workspace_bytes, 106 adds fp4_mx_moe_forward_noalloc and
+ * fp4_mx_moe_static_scratch_bytes. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

@@ -56,7 +56,7 @@ def test_status_strings(lib):
     for code in range(1, 11):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 105
+    assert lib.fp4_abi_version() == 106
 
 
 def test_mx_host_validation(lib):
