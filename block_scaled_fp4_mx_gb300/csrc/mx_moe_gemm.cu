@@ -64,6 +64,7 @@ constexpr int kMmaWarp = kTmaWWarp + 1;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kXBox = 128;                   // activation rows per TMA box
+constexpr int kPrefixExperts = 1024;         // largest expert count of the compact item list
 constexpr int kXBoxBytes = kXBox * kK * 2;  // 16 KiB
 
 template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_, bool kGateUp_ = false>
@@ -71,14 +72,19 @@ struct TmemCfg {
     static constexpr int kTok = kTok_;        // tokens per item (MMA N)
     static constexpr int kMTw = kMTw_;        // 128-row weight tiles per item
     static constexpr int kAccBufs = kAccBufs_;  // accumulator buffers
-    // gate/up mode: the item's two weight tiles are gate rows n0.. and up rows
-    // n_out + n0.. of the same expert, and the epilogue writes silu(gate) * up
+    // gate/up mode: the epilogue writes silu(gate) * up. With two weight tiles
+    // (kMTw = 2) they are gate rows n0.. and up rows n_out + n0..; with one tile
+    // ("halves") its TMEM lanes 0-63 hold gate rows n0..n0+63 and lanes 64-127 the
+    // matching up rows, and the epilogue warps pass the up half through shared
+    // memory (a warp reads only its own 32 lanes)
     static constexpr bool kGateUp = kGateUp_;
+    static constexpr bool kHalves = kGateUp && kMTw_ == 1;
     // a stage of the operand ring holds one slice's activation tile (shared memory)
     // and its decoded weights (tensor memory) under one full and one empty barrier
     static constexpr int S = kStages_, SR = kStagesRaw_;
     static constexpr int kWRows = kWM * kMTw;
-    static constexpr int kTileCols = kGateUp ? kWM : kWRows;  // output columns per item
+    static constexpr int kTileCols = kHalves ? kWM / 2 : kGateUp ? kWM : kWRows;  // output columns per item
+    static constexpr int kBoxRows = kHalves ? kWM / 2 : kGateUp ? kWM : kWRows;  // rows per weight TMA box
     static constexpr int kWarpsPerSlice = 4 * kMTw;
     static constexpr int kGroups = kDecodeWarps / kWarpsPerSlice;
     // tensor memory: accumulator buffers, then the ring of decoded slices
@@ -90,12 +96,21 @@ struct TmemCfg {
     static constexpr int kRawBytes = kWRows * (kK / 2);
     static constexpr int kOffX = 0;
     static constexpr int kOffRaw = kOffX + S * kXBytes;
-    static constexpr int kOffBar = kOffRaw + SR * kRawBytes;
+    // exchange buffer of the halves epilogue: slots G0, G1 (gate values the up warps
+    // need) and U0, U1 (up values the gate warps need), 64 rows x 8 fp32 each, rows
+    // padded to 48 bytes against bank conflicts
+    static constexpr int kXchgRow = 48;
+    static constexpr int kXchgSlot = (kWM / 2) * kXchgRow;
+    static constexpr int kOffXchg = kOffRaw + SR * kRawBytes;
+    static constexpr int kXchgBytes = kHalves ? 4 * kXchgSlot : 0;
+    static constexpr int kOffBar = kOffXchg + kXchgBytes;
     static constexpr int kNumBars = 2 * (S + SR) + 2 * kAccBufs + 1;
-    static constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
+    // per-expert prefix of live token slabs (the compact item list), after the
+    // barriers, the TMEM address word and the abort flag
+    static constexpr int kOffPrefix = kOffBar + 8 * kNumBars + 16;
+    static constexpr int kSmemBytes = 1024 + kOffPrefix + 4 * (kPrefixExperts + 1);
     static_assert(kTok == 128 || kTok == 256, "MMA N");
     static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
-    static_assert(!kGateUp || kMTw == 2, "gate/up items pair two weight tiles");
     static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
     static_assert(kAColBase + S * kAStageCols <= (int)kTmemCols, "tensor memory columns");
     static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -104,9 +119,11 @@ struct TmemCfg {
 // Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
 using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
 // More tokens: 256 tokens per item against one weight tile.
-using CfgLarge = TmemCfg<256, 1, 1, 6, 8>;
+using CfgLarge = TmemCfg<256, 1, 1, 6, 6>;
 // Gate/up GEMM of the MoE layer with the activation function in the epilogue.
 using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true>;
+// The same with 256-token slabs: gate and up halves of one weight tile.
+using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 6, true>;
 
 struct Item {
     int64_t row_begin, rows, m0;
@@ -114,7 +131,8 @@ struct Item {
     bool live, bad;
 };
 
-// Item t: weight tile t % n_tiles (fastest), token slab, expert.
+// Item t of the dense list: weight tile t % n_tiles (fastest), token slab, expert
+// (every expert gets the slabs max_rows needs; those past its rows are dead).
 __device__ __forceinline__ Item item_at(int64_t t, int n_tiles, int slabs, int tok, int cols,
                                         const int64_t *__restrict__ offsets, int64_t max_rows,
                                         int64_t total_rows) {
@@ -131,11 +149,50 @@ __device__ __forceinline__ Item item_at(int64_t t, int n_tiles, int slabs, int t
     return it;
 }
 
-// silu(g) * u of two fp32 accumulator words: g / (1 + e^-g) * u in fp32 (e^-g
-// from expf; a gate below about -88 gives e^-g = inf and a signed zero).
+// Item t of the compact list (live items only): global slab s = t / n_tiles, found
+// in the per-expert slab prefix by binary search (an expert with no slab has the
+// same prefix as the next one; the last expert with prefix <= s owns slab s).
+__device__ __forceinline__ Item item_compact(int64_t t, int n_tiles, int tok, int cols,
+                                             const int32_t *prefix, int experts,
+                                             const int64_t *__restrict__ offsets) {
+    Item it;
+    const int64_t s = t / n_tiles;
+    it.n0 = (int)(t - s * n_tiles) * cols;
+    int lo = 0, hi = experts;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= s) lo = mid; else hi = mid;
+    }
+    it.expert = lo;
+    it.m0 = (s - prefix[lo]) * tok;
+    it.row_begin = __ldg(offsets + lo);
+    it.rows = __ldg(offsets + lo + 1) - it.row_begin;
+    it.live = true;
+    it.bad = false;
+    return it;
+}
+
+// Barrier 1 across the epilogue warpgroup (128 threads) that also ORs a flag over
+// them: every participant gets the same answer, so all four warps leave a loop
+// together (no warp is left waiting at a barrier the others abandoned).
+__device__ __forceinline__ bool epi_barrier_any(bool flag) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\tsetp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.or.pred pout, 1, 128, pin;\n\tselp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(any)
+        : "r"((uint32_t)flag)
+        : "memory");
+    return any != 0;
+}
+
+// silu(g) * u of two fp32 accumulator words: g / (1 + e^-g) * u in fp32 with the
+// fast exponential and division intrinsics (relative error well below 2^-15 of the
+// result, far under the bf16 rounding that follows; a gate below about -87 gives
+// e^-g = inf and a signed zero).
 __device__ __forceinline__ float silu_mul(uint32_t gate_bits, uint32_t up_bits) {
     const float g = __uint_as_float(gate_bits);
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), __uint_as_float(up_bits));
+    return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), __uint_as_float(up_bits));
 }
 
 template <class C>
@@ -159,21 +216,46 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     auto empty_raw = [&](int s) { return bars + 8u * (2 * S + SR + s); };
     auto acc_full = [&](int b) { return bars + 8u * (2 * (S + SR) + b); };
     auto acc_empty = [&](int b) { return bars + 8u * (2 * (S + SR) + C::kAccBufs + b); };
-    const uint32_t drain_bar = bars + 8u * (C::kNumBars - 1);
+    const uint32_t drain_bar = bars + 8u * (2 * (S + SR) + 2 * C::kAccBufs);
+    // halves epilogue: exchange slots 0, 1 hold gate values, 2, 3 up values
+    const uint32_t xchg = base + C::kOffXchg;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kNumBars);
     volatile uint32_t *abort_flag = tmem_slot + 1;
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + C::kOffPrefix);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int n_tiles = (n_out + C::kTileCols - 1) / C::kTileCols;
     const int slabs = (int)((max_rows + kTok - 1) / kTok);
-    const int64_t n_items = (int64_t)experts * slabs * n_tiles;
     const int nk = (k + kK - 1) / kK;
     const int scale_pitch = k / 32;
-    auto item = [&](int64_t t) {
-        return item_at(t, n_tiles, slabs, kTok, C::kTileCols, expert_offsets, max_rows, total_rows);
-    };
+    // up to kPrefixExperts experts the CTAs walk live items only; beyond, every
+    // expert gets max_rows' slabs and dead items are skipped
+    const bool compact = experts <= kPrefixExperts;
+    if (compact && warp == 1) {
+        // lane l owns experts [l * per, (l + 1) * per): its run of slab counts, then a
+        // warp scan of the run totals; an expert with inconsistent offsets gets no slab
+        const int per = (experts + 31) / 32;
+        const int e0 = lane * per, e1 = e0 + per < experts ? e0 + per : experts;
+        int32_t run = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int64_t rb = __ldg(expert_offsets + e), end = __ldg(expert_offsets + e + 1);
+            const int64_t rows = end - rb;
+            const bool ok = rb >= 0 && rows >= 0 && rows <= max_rows && end <= total_rows;
+            if (!ok && blockIdx.x == 0) atomicExch(status, FP4_ERR_SHAPE);
+            prefix[e] = run;
+            run += ok ? (int32_t)((rows + kTok - 1) / kTok) : 0;
+        }
+        int32_t incl = run;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        for (int e = e0; e < e1; ++e) prefix[e] += incl - run;
+        if (lane == 31) prefix[experts] = incl;
+    }
     // tokens of an item that are computed: a slab whose live rows fit in 128 takes
     // N = 128 MMAs and one activation box per slice
     auto tok_live = [&](const Item &it) {
@@ -211,6 +293,13 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int64_t n_items = compact ? (int64_t)prefix[experts] * n_tiles
+                                    : (int64_t)experts * slabs * n_tiles;
+    auto item = [&](int64_t t) {
+        return compact ? item_compact(t, n_tiles, kTok, C::kTileCols, prefix, experts, expert_offsets)
+                       : item_at(t, n_tiles, slabs, kTok, C::kTileCols, expert_offsets, max_rows,
+                                 total_rows);
+    };
 
     if (warp < kDecodeWarps) {
         // ---- decoders: slice g (counted across this CTA's items) belongs to group g % kGroups ----
@@ -231,8 +320,9 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const Item it = item(t);
             if (!it.live) continue;
             // the weight row this thread decodes (within the expert) and whether it exists
-            const int i_tile = r - mt * kWM;
-            const int wr = C::kGateUp ? mt * n_out + it.n0 + i_tile : it.n0 + r;
+            const int i_tile = C::kHalves ? (r & (kWM / 2 - 1)) : r - mt * kWM;
+            const int half = C::kHalves ? r / (kWM / 2) : mt;  // 0 gate, 1 up in gate/up mode
+            const int wr = C::kGateUp ? half * n_out + it.n0 + i_tile : it.n0 + r;
             const bool row_ok = C::kGateUp ? it.n0 + i_tile < n_out : wr < n_out;
             const uint8_t *srow = w_scales + ((int64_t)it.expert * n_rows + wr) * scale_pitch;
             // the row's two E8M0 bytes of slice kt; those of the group's next slice
@@ -292,6 +382,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     } else if (warp < kEpiWarp0 + kEpiWarps) {
         // ---- epilogue: accumulator (weight rows x tokens) -> bf16 output ----
         const int quarter = warp & 3;
+        uint32_t xchg_uses = 0;  // exchange slots used so far (halves mode)
         uint32_t use[2] = {0, 0};
         uint32_t j = 0;  // live items so far
         bool stop = false;
@@ -301,13 +392,70 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
             const uint32_t u = b ? use[1] : use[0];
             if (lane == 0 && !mbar_wait_bounded(acc_full(b), u & 1u)) *abort_flag = 1;
-            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+            if (C::kHalves ? epi_barrier_any(*abort_flag != 0)  // the four warps decide together
+                           : __any_sync(0xFFFFFFFFu, *abort_flag != 0))
+                break;
             tc_fence_after();
             const int64_t tok_rows = it.rows - it.m0;  // > 0
             const int n_tok = (int)(tok_rows < kTok ? tok_rows : kTok);
             const int c_end = (n_tok + 31) & ~31;
             const bool odd = lane & 1;
-            if constexpr (C::kGateUp) {
+            if constexpr (C::kHalves) {
+                // warps 0, 1 read the gate half (lanes 0-63), warps 2, 3 the up half of
+                // the same 64 output columns. Per 16-token chunk the gate warps finish
+                // tokens 0-7 and the up warps tokens 8-15: each half posts the other
+                // half's share of its values in an exchange slot, then reads its own
+                const bool up_warp = quarter >= 2;
+                const int row = (quarter & 1) * 32 + lane;  // output column - n0
+                const int col = it.n0 + (quarter & 1) * 32 + (lane & ~1);
+                const bool col_ok = col < n_out;
+                const int t_half = up_warp ? 8 : 0;  // this warp's tokens within a chunk
+                uint16_t *optr = out + (it.row_begin + it.m0 + t_half + (odd ? 1 : 0)) * n_out + col;
+                const int64_t step2 = 2 * (int64_t)n_out;
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * C::kAccCols);
+#pragma unroll 1
+                for (int c0 = 0; c0 < c_end && !stop; c0 += 16) {
+                    const int q = (int)(xchg_uses & 1u);
+                    ++xchg_uses;
+                    const int mine_slot = up_warp ? 2 + q : q;  // where this half posts
+                    const int other_slot = up_warp ? q : 2 + q; // where it reads
+                    uint32_t v[16];
+                    tmem_ld16(taddr + (uint32_t)c0, v);
+                    if (c0 + 16 >= c_end) {  // the buffer is read out
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty(b));
+                    }
+                    // post the other half's tokens (gate warps: 8-15, up warps: 0-7); slot q
+                    // was last read two chunks ago, before the previous chunk's barrier
+                    const uint32_t post = xchg + (uint32_t)(mine_slot * C::kXchgSlot + row * C::kXchgRow);
+                    uint32_t p8[8];  // gate warps post tokens 8-15, up warps tokens 0-7
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) p8[i] = up_warp ? v[i] : v[8 + i];
+                    st_shared_v4(post, make_uint4(p8[0], p8[1], p8[2], p8[3]));
+                    st_shared_v4(post + 16u, make_uint4(p8[4], p8[5], p8[6], p8[7]));
+                    if (epi_barrier_any(*abort_flag != 0)) {  // the posts are visible to all four warps
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t get = xchg + (uint32_t)(other_slot * C::kXchgSlot + row * C::kXchgRow);
+                    const uint4 o0 = lds_v4(get), o1 = lds_v4(get + 16u);
+                    const uint32_t theirs[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+                    const int lim = n_tok - c0 - t_half - (odd ? 1 : 0);
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const uint32_t g0 = up_warp ? theirs[i] : v[i], u0 = up_warp ? v[8 + i] : theirs[i];
+                        const uint32_t g1 = up_warp ? theirs[i + 1] : v[i + 1];
+                        const uint32_t u1 = up_warp ? v[8 + i + 1] : theirs[i + 1];
+                        const uint32_t mine = pack_bf16x2_rn(silu_mul(g0, u0), silu_mul(g1, u1));
+                        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+                        const uint32_t word = odd ? prmt(other, mine, 0x7632u) : prmt(mine, other, 0x5410u);
+                        if (col_ok && i < lim) *reinterpret_cast<uint32_t *>(optr) = word;
+                        optr += step2;
+                    }
+                    optr += 8 * (int64_t)n_out;  // skip the other half's 8 tokens
+                }
+            } else if constexpr (C::kGateUp) {
                 // column c of the output: gate in accumulator tile 0, up in tile 1
                 const int col = it.n0 + quarter * 32 + (lane & ~1);
                 const bool col_ok = col < n_out;
@@ -412,8 +560,8 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 mbar_arrive_expect_tx(full_raw(s), (uint32_t)C::kRawBytes);
                 tma_load_2d(raw_ring + s * C::kRawBytes, &map_w, kt * (kK / 2), w_row, full_raw(s));
                 if (C::kGateUp)  // the matching up rows fill the second half of the stage
-                    tma_load_2d(raw_ring + s * C::kRawBytes + kWM * (kK / 2), &map_w, kt * (kK / 2),
-                                w_row + n_out, full_raw(s));
+                    tma_load_2d(raw_ring + s * C::kRawBytes + C::kBoxRows * (kK / 2), &map_w,
+                                kt * (kK / 2), w_row + n_out, full_raw(s));
                 if (++s == SR) { s = 0; ph ^= 1u; }
             }
         }
@@ -540,7 +688,7 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
     }
     CUtensorMap map_x, map_w;
     err = tmem_tensor_maps(a, total_rows, w_packed, experts, n_rows, k,
-                           C::kGateUp ? kWM : C::kWRows, &map_x, &map_w);
+                           C::kBoxRows, &map_x, &map_w);
     if (err != cudaSuccess) return err;
     const int64_t items = experts * ((max_rows + C::kTok - 1) / C::kTok) *
                           ((n_out + C::kTileCols - 1) / C::kTileCols);
@@ -570,6 +718,9 @@ cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offse
                                   int64_t max_rows, int64_t total_rows, const uint8_t *w1_packed,
                                   const uint8_t *w1_scales, int64_t n, int64_t k, uint16_t *act,
                                   int32_t *status, cudaStream_t stream) {
+    if (max_rows > 128)
+        return launch_tmem<CfgGateUpLarge>(x, expert_offsets, experts, max_rows, total_rows,
+                                           w1_packed, w1_scales, 2 * n, n, k, act, status, stream);
     return launch_tmem<CfgGateUp>(x, expert_offsets, experts, max_rows, total_rows, w1_packed,
                                   w1_scales, 2 * n, n, k, act, status, stream);
 }
