@@ -41,6 +41,9 @@
 //     holds one weight row, i.e. one output column, for 32 tokens), rounds to
 //     bf16, pairs neighbouring columns with one lane exchange and stores 4-byte
 //     words: the 32 lanes of a warp write two 64-byte runs of two output rows.
+//     In the gate/up "halves" layout a warp's lanes i and 16 + i hold the gate
+//     and up rows of one output column, so silu(gate) * up needs one xor-16 lane
+//     exchange per pair of tokens and no shared memory.
 //
 // Every mbarrier wait is bounded: a wait that runs out sets an abort flag that
 // every role polls, and the launch reports FP4_ERR_TIMEOUT in the status word
@@ -74,9 +77,10 @@ struct TmemCfg {
     static constexpr int kAccBufs = kAccBufs_;  // accumulator buffers
     // gate/up mode: the epilogue writes silu(gate) * up. With two weight tiles
     // (kMTw = 2) they are gate rows n0.. and up rows n_out + n0..; with one tile
-    // ("halves") its TMEM lanes 0-63 hold gate rows n0..n0+63 and lanes 64-127 the
-    // matching up rows, and the epilogue warps pass the up half through shared
-    // memory (a warp reads only its own 32 lanes)
+    // ("halves") it holds 64 gate rows and the 64 matching up rows, interleaved
+    // by 16 so that every warp's 32 TMEM lanes hold a gate row and its up row 16
+    // lanes apart: lanes 32q + i and 32q + 16 + i (i < 16) are gate and up rows
+    // n0 + 16q + i, and the epilogue pairs them with one lane exchange
     static constexpr bool kGateUp = kGateUp_;
     static constexpr bool kHalves = kGateUp && kMTw_ == 1;
     // a stage of the operand ring holds one slice's activation tile (shared memory)
@@ -96,14 +100,7 @@ struct TmemCfg {
     static constexpr int kRawBytes = kWRows * (kK / 2);
     static constexpr int kOffX = 0;
     static constexpr int kOffRaw = kOffX + S * kXBytes;
-    // exchange buffer of the halves epilogue: slots G0, G1 (gate values the up warps
-    // need) and U0, U1 (up values the gate warps need), 64 rows x 8 fp32 each, rows
-    // padded to 48 bytes against bank conflicts
-    static constexpr int kXchgRow = 48;
-    static constexpr int kXchgSlot = (kWM / 2) * kXchgRow;
-    static constexpr int kOffXchg = kOffRaw + SR * kRawBytes;
-    static constexpr int kXchgBytes = kHalves ? 4 * kXchgSlot : 0;
-    static constexpr int kOffBar = kOffXchg + kXchgBytes;
+    static constexpr int kOffBar = kOffRaw + SR * kRawBytes;
     static constexpr int kNumBars = 2 * (S + SR) + 2 * kAccBufs + 1;
     // per-expert prefix of live token slabs (the compact item list), after the
     // barriers, the TMEM address word and the abort flag
@@ -172,20 +169,6 @@ __device__ __forceinline__ Item item_compact(int64_t t, int n_tiles, int tok, in
     return it;
 }
 
-// Barrier 1 across the epilogue warpgroup (128 threads) that also ORs a flag over
-// them: every participant gets the same answer, so all four warps leave a loop
-// together (no warp is left waiting at a barrier the others abandoned).
-__device__ __forceinline__ bool epi_barrier_any(bool flag) {
-    uint32_t any;
-    asm volatile(
-        "{\n\t.reg .pred pin, pout;\n\tsetp.ne.u32 pin, %1, 0;\n\t"
-        "bar.red.or.pred pout, 1, 128, pin;\n\tselp.u32 %0, 1, 0, pout;\n\t}"
-        : "=r"(any)
-        : "r"((uint32_t)flag)
-        : "memory");
-    return any != 0;
-}
-
 // silu(g) * u of two fp32 accumulator words: g / (1 + e^-g) * u in fp32 with the
 // fast exponential and division intrinsics (relative error well below 2^-15 of the
 // result, far under the bf16 rounding that follows; a gate below about -87 gives
@@ -217,8 +200,6 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     auto acc_full = [&](int b) { return bars + 8u * (2 * (S + SR) + b); };
     auto acc_empty = [&](int b) { return bars + 8u * (2 * (S + SR) + C::kAccBufs + b); };
     const uint32_t drain_bar = bars + 8u * (2 * (S + SR) + 2 * C::kAccBufs);
-    // halves epilogue: exchange slots 0, 1 hold gate values, 2, 3 up values
-    const uint32_t xchg = base + C::kOffXchg;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kNumBars);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + C::kOffPrefix);
@@ -306,7 +287,10 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         const int quarter = warp & 3;
         const int mt = (warp >> 2) % kMTw;
         const int group = warp / C::kWarpsPerSlice;
-        const int r = mt * kWM + quarter * 32 + lane;  // weight row within the item
+        const int r = mt * kWM + quarter * 32 + lane;  // TMEM lane (M row) within the item
+        // its row of the packed slice in shared memory: the halves layout takes gate
+        // row i from box row i and up row i from box row 64 + i
+        const int raw_r = C::kHalves ? (lane >> 4) * (kWM / 2) + quarter * 16 + (lane & 15) : r;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)C::kAColBase +
                                    (uint32_t)(mt * (kK / 2));
         bool stop = false;
@@ -320,8 +304,8 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const Item it = item(t);
             if (!it.live) continue;
             // the weight row this thread decodes (within the expert) and whether it exists
-            const int i_tile = C::kHalves ? (r & (kWM / 2 - 1)) : r - mt * kWM;
-            const int half = C::kHalves ? r / (kWM / 2) : mt;  // 0 gate, 1 up in gate/up mode
+            const int i_tile = C::kHalves ? quarter * 16 + (lane & 15) : r - mt * kWM;
+            const int half = C::kHalves ? lane >> 4 : mt;  // 0 gate, 1 up in gate/up mode
             const int wr = C::kGateUp ? half * n_out + it.n0 + i_tile : it.n0 + r;
             const bool row_ok = C::kGateUp ? it.n0 + i_tile < n_out : wr < n_out;
             const uint8_t *srow = w_scales + ((int64_t)it.expert * n_rows + wr) * scale_pitch;
@@ -344,7 +328,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     stop = true;
                     break;
                 }
-                const uint32_t raw_row = raw_ring + sr * C::kRawBytes + (uint32_t)r * 32u;
+                const uint32_t raw_row = raw_ring + sr * C::kRawBytes + (uint32_t)raw_r * 32u;
                 const uint4 w0 = lds_v4(raw_row);
                 const uint4 w1 = lds_v4(raw_row + 16u);
                 __syncwarp();
@@ -382,78 +366,59 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     } else if (warp < kEpiWarp0 + kEpiWarps) {
         // ---- epilogue: accumulator (weight rows x tokens) -> bf16 output ----
         const int quarter = warp & 3;
-        uint32_t xchg_uses = 0;  // exchange slots used so far (halves mode)
         uint32_t use[2] = {0, 0};
         uint32_t j = 0;  // live items so far
-        bool stop = false;
-        for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
+        for (int64_t t = blockIdx.x; t < n_items; t += gridDim.x) {
             const Item it = item(t);
             if (!it.live) continue;
             const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
             const uint32_t u = b ? use[1] : use[0];
             if (lane == 0 && !mbar_wait_bounded(acc_full(b), u & 1u)) *abort_flag = 1;
-            if (C::kHalves ? epi_barrier_any(*abort_flag != 0)  // the four warps decide together
-                           : __any_sync(0xFFFFFFFFu, *abort_flag != 0))
-                break;
+            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             tc_fence_after();
             const int64_t tok_rows = it.rows - it.m0;  // > 0
             const int n_tok = (int)(tok_rows < kTok ? tok_rows : kTok);
             const int c_end = (n_tok + 31) & ~31;
             const bool odd = lane & 1;
             if constexpr (C::kHalves) {
-                // warps 0, 1 read the gate half (lanes 0-63), warps 2, 3 the up half of
-                // the same 64 output columns. Per 16-token chunk the gate warps finish
-                // tokens 0-7 and the up warps tokens 8-15: each half posts the other
-                // half's share of its values in an exchange slot, then reads its own
-                const bool up_warp = quarter >= 2;
-                const int row = (quarter & 1) * 32 + lane;  // output column - n0
-                const int col = it.n0 + (quarter & 1) * 32 + (lane & ~1);
+                // lanes 0-15 of a warp hold gate rows and lanes 16-31 the up rows of
+                // the same 16 output columns. Per 32-token chunk the gate lanes finish
+                // tokens 0-15 and the up lanes tokens 16-31: one xor-16 exchange hands
+                // each side the other's values for its tokens
+                const bool up_lane = lane >= 16;
+                const int col = it.n0 + quarter * 16 + (lane & 14);
                 const bool col_ok = col < n_out;
-                const int t_half = up_warp ? 8 : 0;  // this warp's tokens within a chunk
+                const int t_half = up_lane ? 16 : 0;  // this lane's tokens within a chunk
                 uint16_t *optr = out + (it.row_begin + it.m0 + t_half + (odd ? 1 : 0)) * n_out + col;
                 const int64_t step2 = 2 * (int64_t)n_out;
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * C::kAccCols);
 #pragma unroll 1
-                for (int c0 = 0; c0 < c_end && !stop; c0 += 16) {
-                    const int q = (int)(xchg_uses & 1u);
-                    ++xchg_uses;
-                    const int mine_slot = up_warp ? 2 + q : q;  // where this half posts
-                    const int other_slot = up_warp ? q : 2 + q; // where it reads
-                    uint32_t v[16];
-                    tmem_ld16(taddr + (uint32_t)c0, v);
-                    if (c0 + 16 >= c_end) {  // the buffer is read out
+                for (int c0 = 0; c0 < c_end; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + (uint32_t)c0, v);
+                    if (c0 + 32 >= c_end) {  // the buffer is read out
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(acc_empty(b));
                     }
-                    // post the other half's tokens (gate warps: 8-15, up warps: 0-7); slot q
-                    // was last read two chunks ago, before the previous chunk's barrier
-                    const uint32_t post = xchg + (uint32_t)(mine_slot * C::kXchgSlot + row * C::kXchgRow);
-                    uint32_t p8[8];  // gate warps post tokens 8-15, up warps tokens 0-7
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) p8[i] = up_warp ? v[i] : v[8 + i];
-                    st_shared_v4(post, make_uint4(p8[0], p8[1], p8[2], p8[3]));
-                    st_shared_v4(post + 16u, make_uint4(p8[4], p8[5], p8[6], p8[7]));
-                    if (epi_barrier_any(*abort_flag != 0)) {  // the posts are visible to all four warps
-                        stop = true;
-                        break;
-                    }
-                    const uint32_t get = xchg + (uint32_t)(other_slot * C::kXchgSlot + row * C::kXchgRow);
-                    const uint4 o0 = lds_v4(get), o1 = lds_v4(get + 16u);
-                    const uint32_t theirs[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
                     const int lim = n_tok - c0 - t_half - (odd ? 1 : 0);
 #pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        const uint32_t g0 = up_warp ? theirs[i] : v[i], u0 = up_warp ? v[8 + i] : theirs[i];
-                        const uint32_t g1 = up_warp ? theirs[i + 1] : v[i + 1];
-                        const uint32_t u1 = up_warp ? v[8 + i + 1] : theirs[i + 1];
+                    for (int i = 0; i < 16; i += 2) {
+                        // gate lanes send their gate values of tokens 16-31, up lanes
+                        // their up values of tokens 0-15
+                        const uint32_t s0 = up_lane ? v[i] : v[16 + i];
+                        const uint32_t s1 = up_lane ? v[i + 1] : v[16 + i + 1];
+                        const uint32_t r0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+                        const uint32_t r1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+                        const uint32_t g0 = up_lane ? r0 : v[i], u0 = up_lane ? v[16 + i] : r0;
+                        const uint32_t g1 = up_lane ? r1 : v[i + 1], u1 = up_lane ? v[16 + i + 1] : r1;
                         const uint32_t mine = pack_bf16x2_rn(silu_mul(g0, u0), silu_mul(g1, u1));
                         const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
                         const uint32_t word = odd ? prmt(other, mine, 0x7632u) : prmt(mine, other, 0x5410u);
                         if (col_ok && i < lim) *reinterpret_cast<uint32_t *>(optr) = word;
                         optr += step2;
                     }
-                    optr += 8 * (int64_t)n_out;  // skip the other half's 8 tokens
+                    optr += 16 * (int64_t)n_out;  // skip the other side's 16 tokens
                 }
             } else if constexpr (C::kGateUp) {
                 // column c of the output: gate in accumulator tile 0, up in tile 1

@@ -2,7 +2,8 @@
  * fp4mx.h -- C ABI of a GB300 (sm_103a) library that decodes block-scaled FP4
  * (E2M1) data into bf16.
  *
- * Six operations, each one CUDA kernel launch on the caller's stream:
+ * The operations below; each is one CUDA kernel launch on the caller's stream,
+ * except the MoE layer (one memset and six launches):
  *
  *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
  *                             a wrapping 16-bit integer add into the bf16 exponent
@@ -17,6 +18,12 @@
  *   fp4_mx_quantize           bf16 to MXFP4 (the inverse direction of the unpack).
  *   fp4_mx_moe_gemm           grouped MoE GEMM, MXFP4 weights decoded into the
  *                             tensor-core operand (tcgen05), bf16 activations.
+ *   fp4_mx_moe_forward        the whole MoE layer: top-k routing, gate/up GEMM
+ *                             with silu(gate) * up, down GEMM, weighted top-k sum,
+ *                             scratch in a caller-owned workspace
+ *                             (fp4_mx_moe_workspace_bytes).
+ *   fp4_mx_moe_forward_noalloc  the same layer on the library's static device
+ *                             scratch (fp4_mx_moe_static_scratch_bytes).
  *
  * Conventions shared by every entry point:
  *   - Pointers named "device" must be device-accessible CUDA allocations
