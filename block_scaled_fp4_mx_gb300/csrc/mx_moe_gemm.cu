@@ -19,7 +19,11 @@
 // decoded slices can be deep because tensor memory is otherwise idle.
 //
 // One CTA per SM walks a static list of work items (expert, token slab, tile of
-// weight rows; consecutive items share the expert's activation rows in L2). A
+// weight rows; consecutive items share the expert's activation rows in L2). With
+// 256-token slabs an expert's last slab may hold up to 64 more tokens: each K
+// step then issues a second MMA (N = 16..64) on the same decoded weights into
+// accumulator columns 256.., so an expert of 257..320 rows (or 513..576, ...)
+// needs no extra item and no extra decode of its weights. A
 // stage of the operand ring holds one 64-wide K slice: its activation tile in
 // shared memory and its decoded weights in tensor memory, under one "full"
 // barrier (the TMA bytes plus one arrival per decoder warp) and one "empty"
@@ -69,10 +73,17 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kXBox = 128;                   // activation rows per TMA box
 constexpr int kPrefixExperts = 1024;         // largest expert count of the compact item list
 constexpr int kXBoxBytes = kXBox * kK * 2;  // 16 KiB
+constexpr int kXExtBox = 64;                // activation rows per box of a slab's extension
+constexpr int kXExtBytes = kXExtBox * kK * 2;  // 8 KiB
 
-template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_, bool kGateUp_ = false>
+template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_, bool kGateUp_ = false,
+          int kExt_ = 0>
 struct TmemCfg {
     static constexpr int kTok = kTok_;        // tokens per item (MMA N)
+    // an expert's last slab may take up to kExt more tokens (a second MMA per K step
+    // into accumulator columns kTok.., same decoded weights), so that rows just past
+    // a multiple of kTok need no extra item
+    static constexpr int kExt = kExt_;
     static constexpr int kMTw = kMTw_;        // 128-row weight tiles per item
     static constexpr int kAccBufs = kAccBufs_;  // accumulator buffers
     // gate/up mode: the epilogue writes silu(gate) * up. With two weight tiles
@@ -92,11 +103,11 @@ struct TmemCfg {
     static constexpr int kWarpsPerSlice = 4 * kMTw;
     static constexpr int kGroups = kDecodeWarps / kWarpsPerSlice;
     // tensor memory: accumulator buffers, then the ring of decoded slices
-    static constexpr int kAccCols = kMTw * kTok;
+    static constexpr int kAccCols = kMTw * (kTok + kExt);
     static constexpr int kAColBase = kAccBufs * kAccCols;
     static constexpr int kAStageCols = kMTw * (kK / 2);
     // shared memory from a 1024-byte aligned base
-    static constexpr int kXBytes = kTok * kK * 2;
+    static constexpr int kXBytes = (kTok + kExt) * kK * 2;
     static constexpr int kRawBytes = kWRows * (kK / 2);
     static constexpr int kOffX = 0;
     static constexpr int kOffRaw = kOffX + S * kXBytes;
@@ -108,6 +119,7 @@ struct TmemCfg {
     static constexpr int kSmemBytes = 1024 + kOffPrefix + 4 * (kPrefixExperts + 1);
     static_assert(kTok == 128 || kTok == 256, "MMA N");
     static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
+    static_assert(kExt == 0 || (kExt == kXExtBox && kMTw == 1 && kTok == 256), "slab extension");
     static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
     static_assert(kAColBase + S * kAStageCols <= (int)kTmemCols, "tensor memory columns");
     static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -115,12 +127,14 @@ struct TmemCfg {
 
 // Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
 using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
-// More tokens: 256 tokens per item against one weight tile.
-using CfgLarge = TmemCfg<256, 1, 1, 6, 6>;
+// More tokens: 256 tokens per item (an expert's last slab up to 320) against one
+// weight tile.
+using CfgLarge = TmemCfg<256, 1, 1, 5, 5, false, 64>;
 // Gate/up GEMM of the MoE layer with the activation function in the epilogue.
 using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true>;
-// The same with 256-token slabs: gate and up halves of one weight tile.
-using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 6, true>;
+// The same with 256-token slabs (the last up to 320): gate and up halves of one
+// weight tile.
+using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 5, true, 64>;
 
 struct Item {
     int64_t row_begin, rows, m0;
@@ -181,6 +195,7 @@ __device__ __forceinline__ float silu_mul(uint32_t gate_bits, uint32_t up_bits) 
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
 mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
+                        const __grid_constant__ CUtensorMap map_x_ext,
                         const __grid_constant__ CUtensorMap map_w,
                         const int64_t *__restrict__ expert_offsets,
                         const uint8_t *__restrict__ w_scales, int32_t experts, int64_t max_rows,
@@ -226,7 +241,9 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const bool ok = rb >= 0 && rows >= 0 && rows <= max_rows && end <= total_rows;
             if (!ok && blockIdx.x == 0) atomicExch(status, FP4_ERR_SHAPE);
             prefix[e] = run;
-            run += ok ? (int32_t)((rows + kTok - 1) / kTok) : 0;
+            // slabs of kTok tokens, the last one up to kTok + kExt
+            const int64_t n_slabs = rows <= 0 ? 0 : (rows - C::kExt + kTok - 1) / kTok;
+            run += ok ? (int32_t)(n_slabs > 1 ? n_slabs : (rows > 0 ? 1 : 0)) : 0;
         }
         int32_t incl = run;
 #pragma unroll
@@ -237,11 +254,16 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         for (int e = e0; e < e1; ++e) prefix[e] += incl - run;
         if (lane == 31) prefix[experts] = incl;
     }
-    // tokens of an item that are computed: a slab whose live rows fit in 128 takes
-    // N = 128 MMAs and one activation box per slice
-    auto tok_live = [&](const Item &it) {
-        return (kTok == 256 && it.rows - it.m0 <= 128) ? 128 : kTok;
+    // tokens of an item: kTok, or what is left of the expert's rows; in the compact
+    // list an expert's last slab takes up to kTok + kExt
+    auto item_tokens = [&](const Item &it) -> int {
+        const int64_t left = it.rows - it.m0;  // > 0 for a live item
+        if (C::kExt > 0 && compact && left <= kTok + C::kExt) return (int)left;
+        return (int)(left < kTok ? left : kTok);
     };
+    // MMA N of the first kTok tokens: a slab whose rows fit in 128 takes N = 128 MMAs
+    // and one activation box per slice
+    auto tok_live = [&](int n_tok) { return (kTok == 256 && n_tok <= 128) ? 128 : kTok; };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -376,8 +398,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             if (lane == 0 && !mbar_wait_bounded(acc_full(b), u & 1u)) *abort_flag = 1;
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             tc_fence_after();
-            const int64_t tok_rows = it.rows - it.m0;  // > 0
-            const int n_tok = (int)(tok_rows < kTok ? tok_rows : kTok);
+            const int n_tok = item_tokens(it);  // > 0
             const int c_end = (n_tok + 31) & ~31;
             const bool odd = lane & 1;
             if constexpr (C::kHalves) {
@@ -492,8 +513,28 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
             const Item it = item(t);
             if (!it.live) continue;
-            const int boxes = tok_live(it) / kXBox;
+            const int n_tok = item_tokens(it);
             const int row0 = (int)(it.row_begin + it.m0);
+            // extended slabs get a loop of their own: this thread is on the critical
+            // path, and a branch for the extension box in the plain loop costs ~10%
+            if (C::kExt > 0 && n_tok > kTok) {
+                for (int kt = 0; kt < nk; ++kt, ++g) {
+                    if (g >= (uint32_t)S && !mbar_wait_bounded(empty(s), ph ^ 1u)) *abort_flag = 1;
+                    if (*abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full(s), (uint32_t)(kTok / kXBox * kXBoxBytes + kXExtBytes));
+                    for (int bx = 0; bx < kTok / kXBox; ++bx)
+                        tma_load_2d(x_ring + s * C::kXBytes + bx * kXBoxBytes, &map_x, kt * kK,
+                                    row0 + bx * kXBox, full(s));
+                    tma_load_2d(x_ring + s * C::kXBytes + kTok / kXBox * kXBoxBytes, &map_x_ext,
+                                kt * kK, row0 + kTok, full(s));
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+                continue;
+            }
+            const int boxes = tok_live(n_tok) / kXBox;
             for (int kt = 0; kt < nk; ++kt, ++g) {
                 if (g >= (uint32_t)S && !mbar_wait_bounded(empty(s), ph ^ 1u)) *abort_flag = 1;
                 if (*abort_flag) {
@@ -547,26 +588,51 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const Item it = item(t);
             if (it.bad) atomicExch(status, FP4_ERR_SHAPE);
             if (!it.live) continue;
-            const uint32_t idesc = tok_live(it) == kTok ? idesc_full : idesc_half;
+            const int n_tok = item_tokens(it);
+            const uint32_t idesc = tok_live(n_tok) == kTok ? idesc_full : idesc_half;
+            // an extended slab: tokens kTok.. (N rounded up to 16) into columns kTok..
+            const int n_ext = C::kExt > 0 && n_tok > kTok ? (n_tok - kTok + 15) & ~15 : 0;
+            const uint32_t idesc_ext = instr_desc_bf16<kWM, 16>() + ((uint32_t)(n_ext - 16) >> 3 << 17);
             const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
             const uint32_t u = b ? use[1] : use[0];
             // the buffer's previous item must have been read out
             if (u > 0 && !mbar_wait_bounded(acc_empty(b), (u - 1u) & 1u)) *abort_flag = 1;
             const uint32_t d_col = tmem + (uint32_t)(b * C::kAccCols);
-            for (int kt = 0; kt < nk; ++kt) {
-                if (!ready && !mbar_wait_bounded(full(st), ph)) {
-                    *abort_flag = 1;
-                    break;
+            // separate K loops for extended and plain slabs: every instruction of this
+            // thread is tensor-pipe idle time, so the common loop carries no extra branch
+            if (C::kExt > 0 && n_ext > 0) {
+                for (int kt = 0; kt < nk; ++kt) {
+                    if (!ready && !mbar_wait_bounded(full(st), ph)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int st_next = st + 1 == S ? 0 : st + 1;
+                    const uint32_t ph_next = st + 1 == S ? ph ^ 1u : ph;
+                    const uint64_t x_desc = x_desc0 + (uint64_t)(st * (C::kXBytes >> 4));
+                    ready = mma_slice_tmem_a_ext(d_col, a_col0 + (uint32_t)(st * C::kAStageCols), x_desc,
+                                                 idesc, d_col + (uint32_t)kTok,
+                                                 x_desc + (uint64_t)(kTok * kK * 2 >> 4), idesc_ext,
+                                                 kt > 0 ? 1u : 0u, empty(st), full(st_next), ph_next);
+                    st = st_next;
+                    ph = ph_next;
                 }
-                tc_fence_after();
-                const int st_next = st + 1 == S ? 0 : st + 1;
-                const uint32_t ph_next = st + 1 == S ? ph ^ 1u : ph;
-                ready = mma_slice_tmem_a<kMTw, kTok>(
-                    d_col, a_col0 + (uint32_t)(st * C::kAStageCols),
-                    x_desc0 + (uint64_t)(st * (C::kXBytes >> 4)), idesc, kt > 0 ? 1u : 0u,
-                    empty(st), full(st_next), ph_next);
-                st = st_next;
-                ph = ph_next;
+            } else {
+                for (int kt = 0; kt < nk; ++kt) {
+                    if (!ready && !mbar_wait_bounded(full(st), ph)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int st_next = st + 1 == S ? 0 : st + 1;
+                    const uint32_t ph_next = st + 1 == S ? ph ^ 1u : ph;
+                    ready = mma_slice_tmem_a<kMTw, kTok>(
+                        d_col, a_col0 + (uint32_t)(st * C::kAStageCols),
+                        x_desc0 + (uint64_t)(st * (C::kXBytes >> 4)), idesc, kt > 0 ? 1u : 0u,
+                        empty(st), full(st_next), ph_next);
+                    st = st_next;
+                    ph = ph_next;
+                }
             }
             if (*abort_flag) {
                 stop = true;
@@ -604,12 +670,13 @@ int sm_count() {
     return count;
 }
 
-// Tensor maps of the activations [total_rows, k] bf16 (64 x 128 boxes, 128-byte
-// swizzle; rows past total_rows and columns past k read as zero) and of the packed
+// Tensor maps of the activations [total_rows, k] bf16 (64 x 128 boxes and, for
+// slab extensions, 64 x 64 boxes; 128-byte swizzle; rows past total_rows and
+// columns past k read as zero) and of the packed
 // weights [experts * n_rows, k / 2] uint8 (32-byte x box_rows boxes, no swizzle).
 cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_t *w_packed,
                              int64_t experts, int64_t n_rows, int64_t k, int box_rows, CUtensorMap *map_x,
-                             CUtensorMap *map_w) {
+                             CUtensorMap *map_x_ext, CUtensorMap *map_w) {
     EncodeTiled encode = tensor_map_encoder();
     if (encode == nullptr) return cudaErrorNotSupported;
     const cuuint32_t elem_strides[2] = {1, 1};
@@ -619,6 +686,12 @@ cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_
         const cuuint32_t box[2] = {kK, kXBox};
         if (encode(map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a), dims,
                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        const cuuint32_t box_ext[2] = {kK, kXExtBox};
+        if (encode(map_x_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a), dims,
+                   strides, box_ext, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -651,9 +724,9 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
         if (err != cudaSuccess) return err;
         configured_device = device;
     }
-    CUtensorMap map_x, map_w;
+    CUtensorMap map_x, map_x_ext, map_w;
     err = tmem_tensor_maps(a, total_rows, w_packed, experts, n_rows, k,
-                           C::kBoxRows, &map_x, &map_w);
+                           C::kBoxRows, &map_x, &map_x_ext, &map_w);
     if (err != cudaSuccess) return err;
     const int64_t items = experts * ((max_rows + C::kTok - 1) / C::kTok) *
                           ((n_out + C::kTileCols - 1) / C::kTileCols);
@@ -661,7 +734,7 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(items < sms ? items : sms);
     mx_moe_gemm_kernel<C><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        map_x, map_w, expert_offsets, w_scales, (int32_t)experts, max_rows, total_rows,
+        map_x, map_x_ext, map_w, expert_offsets, w_scales, (int32_t)experts, max_rows, total_rows,
         (int32_t)n_rows, (int32_t)n_out, (int32_t)k, out, status);
     return cudaGetLastError();
 }

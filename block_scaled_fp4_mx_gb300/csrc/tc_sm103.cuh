@@ -124,6 +124,41 @@ __device__ __forceinline__ uint32_t mma_slice_tmem_a(uint32_t d_tmem, uint32_t a
     return ready;
 }
 
+// The single-tile slice of mma_slice_tmem_a with a second accumulator: each K step
+// also multiplies the same A columns with a second B operand (`b2_desc`, e.g. the
+// activation rows past the first N) into `d2_tmem` with its own instruction
+// descriptor `idesc2` (a smaller N).
+__device__ __forceinline__ uint32_t mma_slice_tmem_a_ext(uint32_t d_tmem, uint32_t a_tmem,
+                                                         uint64_t b_desc, uint32_t idesc,
+                                                         uint32_t d2_tmem, uint64_t b2_desc,
+                                                         uint32_t idesc2, uint32_t accumulate,
+                                                         uint32_t empty_bar, uint32_t next_bar,
+                                                         uint32_t next_phase) {
+    uint32_t ready;
+    asm volatile(
+        "{\n\t.reg .pred pr, p0, pt;\n\t.reg .b64 b1, b2, b3, c1, c2, c3;\n\t.reg .b32 a1, a2, a3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pr, [%10], %11;\n\t"
+        "setp.ne.b32 p0, %8, 0;\n\tsetp.eq.b32 pt, %8, %8;\n\t"
+        "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+        "add.u64 c1, %6, 2;\n\tadd.u64 c2, %6, 4;\n\tadd.u64 c3, %6, 6;\n\t"
+        "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%5], [%2], %6, %7, p0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%5], [a1], c1, %7, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%5], [a2], c2, %7, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%5], [a3], c3, %7, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t"
+        "selp.u32 %0, 1, 0, pr;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(d2_tmem), "l"(b2_desc),
+          "r"(idesc2), "r"(accumulate), "r"(empty_bar), "r"(next_bar), "r"(next_phase)
+        : "memory");
+    return ready;
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      bar)

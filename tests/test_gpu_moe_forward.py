@@ -164,6 +164,17 @@ def test_small_layers(oracle_impl, tokens, k, n, experts, topk):
     check(oracle_impl, make_layer(tokens, k, n, experts, topk, seed=tokens + k + n))
 
 
+def test_extended_last_slabs(oracle_impl):
+    """Experts holding 300, 320, 321, 577 and 40 rows (top-1 routing fixed per
+    token): last slabs extended past 256 tokens by up to 64 in both GEMMs, the
+    gate/up epilogue reading accumulator columns 256-319."""
+    counts = [300, 320, 321, 577, 40]
+    L = make_layer(sum(counts), 64, 96, len(counts), 1, seed=53)
+    rng = np.random.default_rng(54)
+    L["ids"] = rng.permutation(np.repeat(np.arange(len(counts)), counts)).astype(np.int32)[:, None]
+    check(oracle_impl, L)
+
+
 def test_gpt_oss_like_layer(oracle_impl):
     """Hidden 2880, intermediate 2880, 4 experts, top-4 of 64 tokens."""
     check(oracle_impl, make_layer(64, 2880, 2880, 4, 4, seed=31))

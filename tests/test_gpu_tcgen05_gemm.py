@@ -108,6 +108,16 @@ def test_256_token_slabs(oracle_impl, rows, n, k):
     run_case(oracle_impl, rows, n, k, seed=sum(rows) + k)
 
 
+@pytest.mark.parametrize("rows,n,k", [([320, 321, 576, 577, 33, 260], 192, 320),
+                                      ([289, 304, 316, 830], 96, 2880)])
+def test_extended_last_slabs(oracle_impl, rows, n, k):
+    """An expert's last slab takes up to 64 rows past 256 with a second MMA per K
+    step: 320 rows in one item (N = 256 + 64), 321 in two (256, then 65 at
+    N = 128), 576 in two (256, 256 + 64), 577 in three; extensions of 4 to 60
+    rows (second MMA N = 16 to 64)."""
+    run_case(oracle_impl, rows, n, k, seed=sum(rows) + k)
+
+
 def test_256_token_slabs_rows_beyond_capacity_flagged(oracle_impl):
     """The capacity check holds with 256-token slabs as well."""
     k, n = 64, 64
