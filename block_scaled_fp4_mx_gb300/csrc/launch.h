@@ -46,7 +46,7 @@ cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offse
 // The MoE layer: routing, gate/up GEMM with silu(gate) * up, down GEMM, top-k
 // weighted sum. Byte offsets of its scratch arrays in the caller's workspace.
 struct MoeWorkspace {
-    uint64_t counts, cursors, offsets, pos, xg, act, y, total;
+    uint64_t counts, ticket, cursors, offsets, pos, xg, act, y, total;
 };
 MoeWorkspace moe_workspace_layout(int64_t tokens, int64_t topk, int64_t experts, int64_t n,
                                   int64_t k);

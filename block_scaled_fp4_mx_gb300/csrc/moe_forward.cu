@@ -4,13 +4,14 @@
 // pull 51583": the CPU test runs ops.fused_experts_cpu with MXFP4 experts):
 // tokens pick top-k experts, each expert runs gate/up GEMM -> silu(gate) * up ->
 // down GEMM, and a token's output is the weighted sum over its slots. Here:
-//   1. moe_count_kernel   histogram of the slots' expert ids (bad ids flagged);
-//   2. moe_scan_kernel    exclusive prefix -> per-expert row offsets, cursors;
-//   3. moe_scatter_kernel each valid slot takes a row of its expert's segment and
+//   1. moe_route_kernel   histogram of the slots' expert ids (bad ids flagged), and
+//                         in the last block to finish the exclusive prefix ->
+//                         per-expert row offsets and cursors;
+//   2. moe_scatter_kernel each valid slot takes a row of its expert's segment and
 //                         copies its token's activations there (one warp per slot);
-//   4. gate/up GEMM       the tensor-memory GEMM in gate/up mode: act = bf16(silu(g) * u);
-//   5. down GEMM          the same kernel: y = bf16(act @ W2_e^T);
-//   6. moe_combine_kernel out[m] = bf16(sum_j w[m, j] * y[row of slot j]) in fp32,
+//   3. gate/up GEMM       the tensor-memory GEMM in gate/up mode: act = bf16(silu(g) * u);
+//   4. down GEMM          the same kernel: y = bf16(act @ W2_e^T);
+//   5. moe_combine_kernel out[m] = bf16(sum_j w[m, j] * y[row of slot j]) in fp32,
 //                         slots in order j = 0, 1, ... (one warp per token).
 // The order of rows inside an expert's segment follows atomic arrival and is not
 // fixed, but every row is computed on its own (no value depends on its position)
@@ -29,37 +30,54 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
+// Histogram of the slots' expert ids, then (in the last block to finish) the
+// exclusive prefix -> per-expert row offsets and scatter cursors. Each block counts
+// into shared memory first (one global atomic per expert and block); the block
+// that takes the last ticket scans. No block waits for another: the ticket only
+// decides which one scans. An expert with more rows than the capacity is flagged;
+// the scatter then drops its slots. counts[] and *ticket are zero on entry.
+constexpr int kLocalExperts = 4096;  // shared-memory histogram up to this many experts
 __global__ void __launch_bounds__(kThreads)
-moe_count_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t experts,
-                 int32_t *__restrict__ counts, int32_t *__restrict__ status) {
-    for (int64_t p = (int64_t)blockIdx.x * kThreads + threadIdx.x; p < pairs;
-         p += (int64_t)gridDim.x * kThreads) {
+moe_route_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t experts, int64_t max_rows,
+                 int32_t *__restrict__ counts, uint32_t *__restrict__ ticket,
+                 int64_t *__restrict__ offsets, int32_t *__restrict__ cursors,
+                 int32_t *__restrict__ status) {
+    extern __shared__ int32_t hist[];  // experts entries when experts <= kLocalExperts
+    __shared__ int64_t part[kThreads];
+    __shared__ bool last;
+    const int t = threadIdx.x;
+    const bool local = experts <= kLocalExperts;
+    if (local)
+        for (int e = t; e < experts; e += kThreads) hist[e] = 0;
+    __syncthreads();
+    for (int64_t p = (int64_t)blockIdx.x * kThreads + t; p < pairs; p += (int64_t)gridDim.x * kThreads) {
         const int32_t e = ids[p];
         if (e < 0 || e >= experts)
             atomicExch(status, FP4_ERR_INDEX);
+        else if (local)
+            atomicAdd(hist + e, 1);
         else
             atomicAdd(counts + e, 1);
     }
-}
-
-// One block of 1024 threads: thread t sums a contiguous run of experts, the block
-// scans the run sums, and each thread writes its run's offsets. An expert with
-// more rows than the capacity is flagged; the scatter then drops its slots.
-constexpr int kScanThreads = 1024;
-__global__ void __launch_bounds__(kScanThreads)
-moe_scan_kernel(const int32_t *__restrict__ counts, int32_t experts, int64_t max_rows,
-                int64_t *__restrict__ offsets, int32_t *__restrict__ cursors,
-                int32_t *__restrict__ status) {
-    __shared__ int64_t part[kScanThreads];
-    const int t = threadIdx.x;
-    const int per = (experts + kScanThreads - 1) / kScanThreads;
+    __syncthreads();
+    if (local)
+        for (int e = t; e < experts; e += kThreads)
+            if (hist[e] != 0) atomicAdd(counts + e, hist[e]);
+    __threadfence();  // this block's counts are visible before its ticket
+    __syncthreads();
+    if (t == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    // thread t sums a contiguous run of experts, the block scans the run sums
+    const int per = (experts + kThreads - 1) / kThreads;
     const int e0 = t * per;
     const int e1 = e0 + per < experts ? e0 + per : experts;
     int64_t sum = 0;
-    for (int e = e0; e < e1; ++e) sum += counts[e];
+    for (int e = e0; e < e1; ++e) sum += __ldcg(counts + e);
     part[t] = sum;
     __syncthreads();
-    for (int d = 1; d < kScanThreads; d <<= 1) {  // inclusive Hillis-Steele scan
+    for (int d = 1; d < kThreads; d <<= 1) {  // inclusive Hillis-Steele scan
         const int64_t v = t >= d ? part[t - d] : 0;
         __syncthreads();
         part[t] += v;
@@ -67,12 +85,13 @@ moe_scan_kernel(const int32_t *__restrict__ counts, int32_t experts, int64_t max
     }
     int64_t run = part[t] - sum;  // exclusive prefix of this thread's run
     for (int e = e0; e < e1; ++e) {
+        const int32_t c = __ldcg(counts + e);
         offsets[e] = run;
         cursors[e] = (int32_t)run;
-        if (counts[e] > max_rows) atomicExch(status, FP4_ERR_SHAPE);
-        run += counts[e];
+        if (c > max_rows) atomicExch(status, FP4_ERR_SHAPE);
+        run += c;
     }
-    if (t == kScanThreads - 1) offsets[experts] = part[t];
+    if (t == kThreads - 1) offsets[experts] = part[t];
 }
 
 // One warp per slot p = m * topk + j.
@@ -94,10 +113,40 @@ moe_scatter_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t topk,
     if (slot < 0) return;
     const uint4 *src = a + (p / topk) * row_vecs;
     uint4 *dst = xg + (int64_t)slot * row_vecs;
-    for (int v = lane; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
+    for (int v0 = lane; v0 < row_vecs; v0 += 4 * 32) {  // four 16-byte loads in flight per lane
+        uint4 r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (v0 + 32 * i < row_vecs) r[i] = __ldg(src + v0 + 32 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (v0 + 32 * i < row_vecs) dst[v0 + 32 * i] = r[i];
+    }
 }
 
 // One warp per token: 8 output columns (one 16-byte vector) per lane per step.
+// The token's slot rows and weights are read once; up to kCombineSlots slots all
+// vectors of a step are loaded before the sum, which still adds slot 0, 1, ... in
+// that order (a slot dropped by the scatter is skipped, not added as zero).
+constexpr int kCombineSlots = 8;
+__device__ __forceinline__ void combine_add(float (&acc)[8], float w, const uint4 &q) {
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, __uint_as_float(words[i] << 16)));
+        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, __uint_as_float(words[i] & 0xFFFF0000u)));
+    }
+}
+
+__device__ __forceinline__ uint4 combine_pack(const float (&acc)[8]) {
+    uint4 o;
+    o.x = pack_bf16x2_rn(acc[0], acc[1]);
+    o.y = pack_bf16x2_rn(acc[2], acc[3]);
+    o.z = pack_bf16x2_rn(acc[4], acc[5]);
+    o.w = pack_bf16x2_rn(acc[6], acc[7]);
+    return o;
+}
+
 __global__ void __launch_bounds__(kThreads)
 moe_combine_kernel(const int32_t *__restrict__ pos, const float *__restrict__ weights,
                    int32_t topk, int64_t tokens, const uint4 *__restrict__ y, int32_t row_vecs,
@@ -105,27 +154,42 @@ moe_combine_kernel(const int32_t *__restrict__ pos, const float *__restrict__ we
     const int64_t m = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (m >= tokens) return;
     const int lane = threadIdx.x & 31;
-    for (int v = lane; v < row_vecs; v += 32) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < topk; ++j) {
-            const int32_t s = __ldg(pos + m * topk + j);
-            if (s < 0) continue;
-            const float w = __ldg(weights + m * topk + j);
-            const uint4 q = __ldg(y + (int64_t)s * row_vecs + v);
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, __uint_as_float(words[i] << 16)));
-                acc[2 * i + 1] =
-                    __fadd_rn(acc[2 * i + 1], __fmul_rn(w, __uint_as_float(words[i] & 0xFFFF0000u)));
+    if (topk > kCombineSlots) {
+        for (int v = lane; v < row_vecs; v += 32) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < topk; ++j) {
+                const int32_t s = __ldg(pos + m * topk + j);
+                if (s >= 0) combine_add(acc, __ldg(weights + m * topk + j), __ldg(y + (int64_t)s * row_vecs + v));
             }
+            out[m * row_vecs + v] = combine_pack(acc);
         }
-        uint4 o;
-        o.x = pack_bf16x2_rn(acc[0], acc[1]);
-        o.y = pack_bf16x2_rn(acc[2], acc[3]);
-        o.z = pack_bf16x2_rn(acc[4], acc[5]);
-        o.w = pack_bf16x2_rn(acc[6], acc[7]);
-        out[m * row_vecs + v] = o;
+        return;
+    }
+    // lane j < topk reads slot j's row and weight; every lane takes them by shuffle
+    int32_t s_lane = -1;
+    float w_lane = 0.f;
+    if (lane < topk) {
+        s_lane = __ldg(pos + m * topk + lane);
+        w_lane = __ldg(weights + m * topk + lane);
+    }
+    const uint4 *rows[kCombineSlots];
+    float w[kCombineSlots];
+#pragma unroll
+    for (int j = 0; j < kCombineSlots; ++j) {
+        const int32_t s = __shfl_sync(0xFFFFFFFFu, s_lane, j);
+        w[j] = __shfl_sync(0xFFFFFFFFu, w_lane, j);
+        rows[j] = (j < topk && s >= 0) ? y + (int64_t)s * row_vecs : nullptr;
+    }
+    for (int v = lane; v < row_vecs; v += 32) {
+        uint4 q[kCombineSlots];
+#pragma unroll
+        for (int j = 0; j < kCombineSlots; ++j)
+            if (rows[j] != nullptr) q[j] = __ldg(rows[j] + v);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < kCombineSlots; ++j)
+            if (rows[j] != nullptr) combine_add(acc, w[j], q[j]);
+        out[m * row_vecs + v] = combine_pack(acc);
     }
 }
 
@@ -137,7 +201,8 @@ MoeWorkspace moe_workspace_layout(int64_t tokens, int64_t topk, int64_t experts,
     const uint64_t pairs = (uint64_t)tokens * (uint64_t)topk;
     MoeWorkspace w;
     w.counts = 0;
-    w.cursors = up(w.counts + 4u * (uint64_t)experts);
+    w.ticket = w.counts + 4u * (uint64_t)experts;  // zeroed together with the counts
+    w.cursors = up(w.ticket + 4u);
     w.offsets = up(w.cursors + 4u * (uint64_t)experts);
     w.pos = up(w.offsets + 8u * (uint64_t)(experts + 1));
     w.xg = up(w.pos + 4u * pairs);
@@ -156,6 +221,7 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
     const MoeWorkspace L = moe_workspace_layout(tokens, topk, experts, n, k);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    uint32_t *ticket = reinterpret_cast<uint32_t *>(ws + L.ticket);
     int32_t *cursors = reinterpret_cast<int32_t *>(ws + L.cursors);
     int64_t *offsets = reinterpret_cast<int64_t *>(ws + L.offsets);
     int32_t *pos = reinterpret_cast<int32_t *>(ws + L.pos);
@@ -163,16 +229,15 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
     uint16_t *act = reinterpret_cast<uint16_t *>(ws + L.act);
     uint16_t *y = reinterpret_cast<uint16_t *>(ws + L.y);
     const int64_t pairs = tokens * topk;
-    cudaError_t err = cudaMemsetAsync(counts, 0, (size_t)experts * 4, stream);
+    cudaError_t err = cudaMemsetAsync(counts, 0, (size_t)(experts + 1) * 4, stream);  // + ticket
     if (err != cudaSuccess) return err;
     {
         const int64_t blocks = (pairs + kThreads - 1) / kThreads;
-        const int grid = (int)(blocks < 4096 ? blocks : 4096);
-        moe_count_kernel<<<grid, kThreads, 0, stream>>>(topk_ids, pairs, (int32_t)experts, counts,
-                                                         status);
+        const int grid = (int)(blocks < 1024 ? blocks : 1024);
+        const size_t hist_bytes = experts <= kLocalExperts ? (size_t)experts * 4 : 0;
+        moe_route_kernel<<<grid, kThreads, hist_bytes, stream>>>(
+            topk_ids, pairs, (int32_t)experts, max_rows, counts, ticket, offsets, cursors, status);
     }
-    moe_scan_kernel<<<1, kScanThreads, 0, stream>>>(counts, (int32_t)experts, max_rows, offsets,
-                                                    cursors, status);
     const int32_t k_vecs = (int32_t)(k / 8);
     moe_scatter_kernel<<<(unsigned)((pairs + kWarps - 1) / kWarps), kThreads, 0, stream>>>(
         topk_ids, pairs, (int32_t)topk, (int32_t)experts, max_rows, counts,
