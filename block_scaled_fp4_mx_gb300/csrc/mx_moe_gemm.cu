@@ -121,6 +121,9 @@ struct TmemCfg {
     static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
     static_assert(kExt == 0 || (kExt == kXExtBox && kMTw == 1 && kTok == 256), "slab extension");
     static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
+    // a decoder group's ring positions advance by kGroups per slice and wrap with
+    // one subtraction, so neither ring may be shorter than kGroups
+    static_assert(kGroups <= S && kGroups <= SR, "ring depth below the decoder group count");
     static_assert(kAColBase + S * kAStageCols <= (int)kTmemCols, "tensor memory columns");
     static_assert(kSmemBytes <= 232448, "shared memory per block");
 };

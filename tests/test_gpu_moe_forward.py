@@ -175,6 +175,12 @@ def test_extended_last_slabs(oracle_impl):
     check(oracle_impl, L)
 
 
+def test_many_experts(oracle_impl):
+    """5000 experts: more than the route kernel's shared-memory histogram holds
+    (global atomics) and more than the GEMMs' compact item list (dense list)."""
+    check(oracle_impl, make_layer(64, 32, 32, 5000, 2, seed=57))
+
+
 def test_gpt_oss_like_layer(oracle_impl):
     """Hidden 2880, intermediate 2880, 4 experts, top-4 of 64 tokens."""
     check(oracle_impl, make_layer(64, 2880, 2880, 4, 4, seed=31))

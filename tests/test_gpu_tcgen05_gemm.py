@@ -118,6 +118,18 @@ def test_extended_last_slabs(oracle_impl, rows, n, k):
     run_case(oracle_impl, rows, n, k, seed=sum(rows) + k)
 
 
+@pytest.mark.parametrize("big", [False, True])
+def test_more_experts_than_the_compact_item_list(oracle_impl, big):
+    """1030 experts, more than the kernel's per-expert slab prefix holds: the CTAs
+    walk the dense item list (every expert gets max_rows' slabs, dead items are
+    skipped, no slab extension). Up to 128 rows (two-tile items), then up to 300
+    (256-token slabs: 300 rows are a 256-token slab and a 44-token one)."""
+    rng = np.random.default_rng(61 + big)
+    rows = rng.integers(0, 4, size=1030)
+    rows[[5, 700]] = [130, 300] if big else [128, 77]
+    run_case(oracle_impl, [int(r) for r in rows], 64, 64, seed=63 + big)
+
+
 def test_256_token_slabs_rows_beyond_capacity_flagged(oracle_impl):
     """The capacity check holds with 256-token slabs as well."""
     k, n = 64, 64
