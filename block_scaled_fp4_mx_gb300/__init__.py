@@ -32,7 +32,7 @@ from ._lib import Status, last_error, library_path, load, status_string  # noqa:
 
 __all__ = ["fp4_mx_unpack", "fp4_mx_unpack_pages", "fp4_mx_quantize", "fp4_mx_moe_gemm",
            "fp4_mx_moe_forward", "fp4_mx_moe_workspace_bytes", "fp4_mx_moe_forward_noalloc",
-           "fp4_mx_moe_static_scratch_bytes",
+           "fp4_mx_moe_static_scratch_bytes", "fp4_wait_selftest",
            "fp4_nv_embedding_gather",
            "fp4_nv_dequant",
            "fp4_status_string",
@@ -362,6 +362,22 @@ def fp4_mx_moe_forward_noalloc(a, topk_ids, topk_weights, w1_packed, w1_scales, 
     if code != Status.OK:
         raise Fp4Error("fp4_mx_moe_forward_noalloc", code)
     return out, status
+
+
+def fp4_wait_selftest(mode, status=None, device="cuda", stream=None):
+    """Run one bounded mbarrier wait of the kind that guards the tensor-core
+    kernels on a barrier nothing arrives on (mode 0: spinning wait, 1: sleeping
+    wait; mode 2: a control whose phase completes). The kernel ends when the wait
+    gives up and sets ``status`` (an int32 CUDA tensor, allocated here as zero when
+    not given) to Status.ERR_TIMEOUT. Returns ``status``."""
+    torch = _torch()
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+    _check_cuda(status, "status", (torch.int32,))
+    code = load().fp4_wait_selftest(int(mode), _ptr(status), _stream_handle(stream, status.device))
+    if code != Status.OK:
+        raise Fp4Error("fp4_wait_selftest", code)
+    return status
 
 
 def fp4_mx_unpack_pages(page_ids, packed_pool, scales_pool, out=None, err_flag=None,

@@ -49,6 +49,7 @@ SIGNATURES = {
     "fp4_mx_moe_forward_noalloc": ([_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                     _i64, _i64, _vp, _vp, _vp], ctypes.c_int),
     "fp4_mx_moe_static_scratch_bytes": ([], ctypes.c_int64),
+    "fp4_wait_selftest": ([ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "fp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "fp4_last_error": ([], ctypes.c_char_p),
     "fp4_abi_version": ([], ctypes.c_int),

@@ -304,6 +304,18 @@ FP4_EXPORT int64_t fp4_mx_moe_static_scratch_bytes(void) {
     return (int64_t)fp4mx::moe_static_scratch_bytes();
 }
 
+FP4_EXPORT fp4_status fp4_wait_selftest(int32_t mode, int32_t *status, fp4_stream_t stream) {
+    clear_error();
+    if (mode < 0 || mode > 2) return FP4_ERR_SHAPE;
+    if (status == nullptr) return FP4_ERR_NULL_PTR;
+    if (misaligned(status, 4)) return FP4_ERR_ALIGN;
+    const void *ptrs[] = {status};
+    const fp4_status s = check_pointers(ptrs, 1);
+    if (s != FP4_OK) return s;
+    const cudaError_t err = fp4mx::launch_wait_selftest(mode, status, (cudaStream_t)stream);
+    return err == cudaSuccess ? FP4_OK : cuda_failure(err, "fp4_wait_selftest launch");
+}
+
 FP4_EXPORT fp4_status fp4_mx_moe_forward_noalloc(
     const uint16_t *a_bf16, const int32_t *topk_ids, const float *topk_weights, int64_t tokens,
     int64_t topk, int64_t experts, int64_t max_rows_per_expert, const uint8_t *w1_packed,
@@ -413,4 +425,4 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 106; }
+FP4_EXPORT int fp4_abi_version(void) { return 107; }

@@ -62,6 +62,10 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
 uint64_t moe_static_scratch_bytes();
 cudaError_t moe_static_scratch(void **address);
 
+// Bounded-wait check (wait_selftest.cu): mode 0 spinning wait, 1 sleeping wait,
+// 2 a wait whose phase completes.
+cudaError_t launch_wait_selftest(int32_t mode, int32_t *status, cudaStream_t stream);
+
 // Paged MXFP4 dequant: num_pages (> 0) pages of page_elems (a positive multiple of
 // 32) codes gathered from a pool by id.
 cudaError_t launch_mx_unpack_pages(const int64_t *page_ids, int64_t num_pages,

@@ -50,12 +50,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
     return ok != 0;
 }
 
-// Bounded wait for phase `phase` of the mbarrier; false when the limit ran out.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Bounded wait for phase `phase` of the mbarrier (polling); false once about
+// 2^29 SM cycles (~0.3 s) have passed without the phase completing. The clock is
+// read only after a first poll fails.
+constexpr long long kWaitCycles = 1ll << 29;
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, phase)) return true;
-    return false;
+    if (mbar_try_wait(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, phase))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// Bounded wait that lets the thread sleep: try_wait with a suspend-time hint
+// (1 ms), so a waiting warp does not take issue slots from the warps beside it
+// until the phase completes; false after about 2^29 SM cycles (~0.3 s).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t phase) {
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(phase), "r"(0x100000u)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
 }
 
 __device__ __forceinline__ void tc_fence_before() {

@@ -307,6 +307,25 @@ fp4_status fp4_mx_moe_forward_noalloc(const uint16_t *a_bf16, const int32_t *top
 int64_t fp4_mx_moe_static_scratch_bytes(void);
 
 /*
+ * fp4_wait_selftest -- check of the bounded waits that guard the tensor-core
+ * kernels (fp4_mx_moe_gemm, fp4_mx_moe_forward): every mbarrier wait in them
+ * gives up after a limit, and the launch then writes FP4_ERR_TIMEOUT to its
+ * status word instead of hanging. This call runs one such wait on a barrier that
+ * nothing arrives on, so that a test can see the limit run out without a fault.
+ *
+ *   mode    0: the polling wait (gives up after about 2^29 SM cycles, ~0.3 s);
+ *           1: the sleeping wait (gives up after about 2^29 SM cycles, ~0.3 s);
+ *           2: control, the phase completes first and *status is left alone;
+ *           other values: FP4_ERR_SHAPE
+ *   status  device, one int32; set to FP4_ERR_TIMEOUT when the wait gives up
+ *           (never cleared by the library)
+ *   stream  CUDA stream the one-warp kernel is enqueued on
+ * Returns FP4_ERR_NULL_PTR / FP4_ERR_ALIGN / FP4_ERR_POINTER for a bad status
+ * pointer, else FP4_OK once the kernel is enqueued.
+ */
+fp4_status fp4_wait_selftest(int32_t mode, int32_t *status, fp4_stream_t stream);
+
+/*
  * fp4_nv_dequant -- dequantise a whole NVFP4 table (every row, in order).
  *
  * The dense counterpart of fp4_nv_embedding_gather: out[r][c] is what the
@@ -340,7 +359,7 @@ const char *fp4_last_error(void);
  * fp4_mx_quantize and FP4_ERR_ALIGN, 103 adds fp4_mx_moe_gemm and FP4_ERR_TIMEOUT,
  * 104 adds fp4_mx_unpack_pages, 105 adds fp4_mx_moe_forward and
  * fp4_mx_moe_workspace_bytes, 106 adds fp4_mx_moe_forward_noalloc and
- * fp4_mx_moe_static_scratch_bytes. */
+ * fp4_mx_moe_static_scratch_bytes, 107 adds fp4_wait_selftest. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

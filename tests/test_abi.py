@@ -56,7 +56,7 @@ def test_status_strings(lib):
     for code in range(1, 11):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 106
+    assert lib.fp4_abi_version() == 107
 
 
 def test_mx_host_validation(lib):
@@ -163,6 +163,16 @@ def test_binding_refuses_cpu_tensors():
                                     torch.zeros(4, 8, dtype=torch.uint8),
                                     torch.zeros(4, 1, dtype=torch.uint8),
                                     torch.ones(1, dtype=torch.float32))
+
+
+def test_wait_selftest_host_validation(lib):
+    """Mode, null and alignment are checked before any CUDA call."""
+    f = lib.fp4_wait_selftest
+    base = 1 << 40
+    assert f(3, base, None) == fp4.Status.ERR_SHAPE
+    assert f(-1, base, None) == fp4.Status.ERR_SHAPE
+    assert f(0, None, None) == fp4.Status.ERR_NULL_PTR
+    assert f(1, base + 2, None) == fp4.Status.ERR_ALIGN
 
 
 def test_moe_forward_host_validation(lib):
