@@ -65,13 +65,6 @@ namespace {
 
 constexpr int kWM = 128;  // weight rows per M tile (TMEM lanes)
 constexpr int kK = 64;    // K per slice
-constexpr int kDecodeWarps = 16;
-constexpr int kEpiWarp0 = kDecodeWarps;
-constexpr int kEpiWarps = 4;
-constexpr int kTmaXWarp = kEpiWarp0 + kEpiWarps;
-constexpr int kTmaWWarp = kTmaXWarp + 1;
-constexpr int kMmaWarp = kTmaWWarp + 1;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kXBox = 128;                   // activation rows per TMA box
 constexpr int kPrefixExperts = 1024;         // largest expert count of the compact item list
@@ -80,8 +73,18 @@ constexpr int kXExtBox = 64;                // activation rows per box of a slab
 constexpr int kXExtBytes = kXExtBox * kK * 2;  // 8 KiB
 
 template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_, bool kGateUp_ = false,
-          int kExt_ = 0>
+          int kExt_ = 0, int kDecodeWarps_ = 16, int kEpiWarps_ = 4>
 struct TmemCfg {
+    // warp roles: decoders, epilogue (a multiple of 4: kEpiWarps / 4 warps share
+    // each TMEM lane quarter and take its chunks in turn), the activation TMA
+    // thread, the weight TMA thread and the MMA thread
+    static constexpr int kDecodeWarps = kDecodeWarps_;
+    static constexpr int kEpiWarp0 = kDecodeWarps;
+    static constexpr int kEpiWarps = kEpiWarps_;
+    static constexpr int kTmaXWarp = kEpiWarp0 + kEpiWarps;
+    static constexpr int kTmaWWarp = kTmaXWarp + 1;
+    static constexpr int kMmaWarp = kTmaWWarp + 1;
+    static constexpr int kThreads = (kMmaWarp + 1) * 32;
     static constexpr int kTok = kTok_;        // tokens per item (MMA N)
     // an expert's last slab may take up to kExt more tokens (a second MMA per K step
     // into accumulator columns kTok.., same decoded weights), so that rows just past
@@ -124,6 +127,7 @@ struct TmemCfg {
     static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
     static_assert(kExt == 0 || (kExt == kXExtBox && kMTw == 1 && kTok == 256), "slab extension");
     static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
+    static_assert(kEpiWarps % 4 == 0 && kDecodeWarps % 4 == 0, "warps per TMEM lane quarter");
     // a decoder group's ring positions advance by kGroups per slice and wrap with
     // one subtraction, so neither ring may be shorter than kGroups
     static_assert(kGroups <= S && kGroups <= SR, "ring depth below the decoder group count");
@@ -134,13 +138,14 @@ struct TmemCfg {
 // Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
 using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
 // More tokens: 256 tokens per item (an expert's last slab up to 320) against one
-// weight tile.
-using CfgLarge = TmemCfg<256, 1, 1, 5, 5, false, 64>;
+// weight tile; 12 decoder warps (3 groups) and 8 epilogue warps, so that the
+// single accumulator is read out twice as fast at the end of an item.
+using CfgLarge = TmemCfg<256, 1, 1, 5, 5, false, 64, 12, 8>;
 // Gate/up GEMM of the MoE layer with the activation function in the epilogue.
 using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true>;
 // The same with 256-token slabs (the last up to 320): gate and up halves of one
 // weight tile.
-using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 5, true, 64>;
+using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 5, true, 64, 12, 8>;
 
 struct Item {
     int64_t row_begin, rows, m0;
@@ -199,7 +204,7 @@ __device__ __forceinline__ float silu_mul(uint32_t gate_bits, uint32_t up_bits) 
 }
 
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(C::kThreads, 1)
 mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_x_ext,
                         const __grid_constant__ CUtensorMap map_w,
@@ -283,7 +288,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         }
         for (int b = 0; b < C::kAccBufs; ++b) {
             mbar_init(acc_full(b), 1);
-            mbar_init(acc_empty(b), kEpiWarps);
+            mbar_init(acc_empty(b), C::kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -312,7 +317,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                                  total_rows);
     };
 
-    if (warp < kDecodeWarps) {
+    if (warp < C::kDecodeWarps) {
         // ---- decoders: slice g (counted across this CTA's items) belongs to group g % kGroups ----
         const int quarter = warp & 3;
         const int mt = (warp >> 2) % kMTw;
@@ -393,9 +398,14 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             }
             g0 += (uint32_t)nk;
         }
-    } else if (warp < kEpiWarp0 + kEpiWarps) {
+    } else if (warp < C::kEpiWarp0 + C::kEpiWarps) {
         // ---- epilogue: accumulator (weight rows x tokens) -> bf16 output ----
+        // kEpiSubs warps share each TMEM lane quarter and take its chunks in turn; a
+        // warp releases the accumulator after its last tcgen05.ld (at once if it has
+        // no chunk), so the next item's MMAs wait for the slowest warp's reads only
+        constexpr int kEpiSubs = C::kEpiWarps / 4;
         const int quarter = warp & 3;
+        const int sub = (warp - C::kEpiWarp0) >> 2;
         uint32_t use[2] = {0, 0};
         uint32_t j = 0;  // live items so far
         for (int64_t t = blockIdx.x; t < n_items; t += gridDim.x) {
@@ -406,9 +416,16 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             if (lane == 0 && !mbar_wait_sleep(acc_full(b), u & 1u)) *abort_flag = 1;
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             tc_fence_after();
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty(b));
+            };
             const int n_tok = item_tokens(it);  // > 0
-            const int c_end = (n_tok + 31) & ~31;
             const bool odd = lane & 1;
+            const int64_t step2 = 2 * (int64_t)n_out;
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * C::kAccCols);
+            uint16_t *const obase = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n_out;
             if constexpr (C::kHalves) {
                 // lanes 0-15 of a warp hold gate rows and lanes 16-31 the up rows of
                 // the same 16 output columns. Per 32-token chunk the gate lanes finish
@@ -418,18 +435,15 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 const int col = it.n0 + quarter * 16 + (lane & 14);
                 const bool col_ok = col < n_out;
                 const int t_half = up_lane ? 16 : 0;  // this lane's tokens within a chunk
-                uint16_t *optr = out + (it.row_begin + it.m0 + t_half + (odd ? 1 : 0)) * n_out + col;
-                const int64_t step2 = 2 * (int64_t)n_out;
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * C::kAccCols);
+                const int chunks = (n_tok + 31) / 32;
+                if (sub >= chunks) release();
 #pragma unroll 1
-                for (int c0 = 0; c0 < c_end; c0 += 32) {
+                for (int q = sub; q < chunks; q += kEpiSubs) {
+                    const int c0 = q * 32;
                     uint32_t v[32];
                     tmem_ld32(taddr + (uint32_t)c0, v);
-                    if (c0 + 32 >= c_end) {  // the buffer is read out
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty(b));
-                    }
+                    if (q + kEpiSubs >= chunks) release();
+                    uint16_t *optr = obase + (int64_t)(c0 + t_half) * n_out + col;
                     const int lim = n_tok - c0 - t_half - (odd ? 1 : 0);
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
@@ -447,65 +461,57 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                         if (col_ok && i < lim) *reinterpret_cast<uint32_t *>(optr) = word;
                         optr += step2;
                     }
-                    optr += 16 * (int64_t)n_out;  // skip the other side's 16 tokens
                 }
             } else if constexpr (C::kGateUp) {
                 // column c of the output: gate in accumulator tile 0, up in tile 1
                 const int col = it.n0 + quarter * 32 + (lane & ~1);
                 const bool col_ok = col < n_out;
-                uint16_t *optr = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n_out + col;
-                const int64_t step2 = 2 * (int64_t)n_out;
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * C::kAccCols);
+                const int chunks = (n_tok + 15) / 16;
+                if (sub >= chunks) release();
 #pragma unroll 1
-                for (int c0 = 0; c0 < c_end; c0 += 16) {
+                for (int q = sub; q < chunks; q += kEpiSubs) {
+                    const int c0 = q * 16;
                     uint32_t gate[16], up[16];
                     tmem_ld16(taddr + (uint32_t)c0, gate);
                     tmem_ld16(taddr + (uint32_t)(kTok + c0), up);
-                    if (c0 + 16 >= c_end) {  // the buffer is read out
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty(b));
-                    }
+                    if (q + kEpiSubs >= chunks) release();
+                    uint16_t *optr = obase + (int64_t)c0 * n_out + col;
                     const int lim = n_tok - c0 - (odd ? 1 : 0);
 #pragma unroll
-                    for (int q = 0; q < 16; q += 2) {
-                        const uint32_t mine = pack_bf16x2_rn(silu_mul(gate[q], up[q]),
-                                                             silu_mul(gate[q + 1], up[q + 1]));
+                    for (int i = 0; i < 16; i += 2) {
+                        const uint32_t mine = pack_bf16x2_rn(silu_mul(gate[i], up[i]),
+                                                             silu_mul(gate[i + 1], up[i + 1]));
                         const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
                         const uint32_t word = odd ? prmt(other, mine, 0x7632u) : prmt(mine, other, 0x5410u);
-                        if (col_ok && q < lim) *reinterpret_cast<uint32_t *>(optr) = word;
+                        if (col_ok && i < lim) *reinterpret_cast<uint32_t *>(optr) = word;
                         optr += step2;
                     }
                 }
-            } else
-#pragma unroll 1
-            for (int mt = 0; mt < kMTw; ++mt) {
+            } else {
                 // lanes 2i and 2i+1 hold output columns c and c+1 (c even); after an
                 // exchange the even lane stores both columns of token t and the odd
-                // lane both columns of token t + 1
-                const int col = it.n0 + mt * kWM + quarter * 32 + (lane & ~1);
-                const bool col_ok = col < n_out;
-                uint16_t *optr = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n_out + col;
-                const int64_t step2 = 2 * (int64_t)n_out;
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
-                                       (uint32_t)(b * C::kAccCols + mt * kTok);
+                // lane both columns of token t + 1. Chunk q is tile q / per_tile.
+                const int per_tile = (n_tok + 31) / 32;
+                const int chunks = kMTw * per_tile;
+                if (sub >= chunks) release();
 #pragma unroll 1
-                for (int c0 = 0; c0 < c_end; c0 += 32) {
+                for (int q = sub; q < chunks; q += kEpiSubs) {
+                    const int mt = kMTw == 1 ? 0 : q / per_tile;
+                    const int c0 = (q - mt * per_tile) * 32;
                     uint32_t acc[32];
-                    tmem_ld32(taddr + (uint32_t)c0, acc);
-                    if (mt == kMTw - 1 && c0 + 32 >= c_end) {  // the buffer is read out
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty(b));
-                    }
-                    const int lim = n_tok - c0 - (odd ? 1 : 0);  // tokens q (even) with q < lim are stored
+                    tmem_ld32(taddr + (uint32_t)(mt * kTok + c0), acc);
+                    if (q + kEpiSubs >= chunks) release();
+                    const int col = it.n0 + mt * kWM + quarter * 32 + (lane & ~1);
+                    const bool col_ok = col < n_out;
+                    uint16_t *optr = obase + (int64_t)c0 * n_out + col;
+                    const int lim = n_tok - c0 - (odd ? 1 : 0);  // tokens i (even) with i < lim are stored
 #pragma unroll
-                    for (int q = 0; q < 32; q += 2) {
+                    for (int i = 0; i < 32; i += 2) {
                         const uint32_t mine =
-                            pack_bf16x2_rn(__uint_as_float(acc[q]), __uint_as_float(acc[q + 1]));
+                            pack_bf16x2_rn(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]));
                         const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
                         const uint32_t word = odd ? prmt(other, mine, 0x7632u) : prmt(mine, other, 0x5410u);
-                        if (col_ok && q < lim) *reinterpret_cast<uint32_t *>(optr) = word;
+                        if (col_ok && i < lim) *reinterpret_cast<uint32_t *>(optr) = word;
                         optr += step2;
                     }
                 }
@@ -513,7 +519,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             if (b) ++use[1]; else ++use[0];
             ++j;
         }
-    } else if (warp == kTmaXWarp && lane == 0) {
+    } else if (warp == C::kTmaXWarp && lane == 0) {
         // ---- TMA: activation tiles ----
         int s = 0;
         uint32_t ph = 0, g = 0;
@@ -556,7 +562,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
         }
-    } else if (warp == kTmaWWarp && lane == 0) {
+    } else if (warp == C::kTmaWWarp && lane == 0) {
         // ---- TMA: packed weight slices ----
         int s = 0;
         uint32_t ph = 0, g = 0;
@@ -579,7 +585,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 if (++s == SR) { s = 0; ph ^= 1u; }
             }
         }
-    } else if (warp == kMmaWarp && lane == 0) {
+    } else if (warp == C::kMmaWarp && lane == 0) {
         // ---- MMA issue ----
         constexpr uint32_t idesc_full = instr_desc_bf16<kWM, kTok>();
         constexpr uint32_t idesc_half = instr_desc_bf16<kWM, 128>();
@@ -741,7 +747,7 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(items < sms ? items : sms);
-    mx_moe_gemm_kernel<C><<<grid, kThreads, C::kSmemBytes, stream>>>(
+    mx_moe_gemm_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
         map_x, map_x_ext, map_w, expert_offsets, w_scales, (int32_t)experts, max_rows, total_rows,
         (int32_t)n_rows, (int32_t)n_out, (int32_t)k, out, status);
     return cudaGetLastError();
