@@ -181,6 +181,27 @@ def test_many_experts(oracle_impl):
     check(oracle_impl, make_layer(64, 32, 32, 5000, 2, seed=57))
 
 
+def test_full_size_layer_sampled_tokens(oracle_impl):
+    """The benchmark's layer at full size (4096 tokens, top-4 of 32 experts, hidden =
+    intermediate = 2880: experts of about 512 +- 22 rows, so 256-token slabs and
+    extended last slabs in both GEMMs) on the GPU; the oracle recomputes 8 tokens,
+    whose outputs depend on nothing else. Those tokens are routed among experts 0-3
+    so that the oracle decodes only four experts' weights."""
+    tokens, k, n, experts, topk, sample = 4096, 2880, 2880, 32, 4, 8
+    L = make_layer(tokens, k, n, experts, topk, seed=61)
+    rng = np.random.default_rng(62)
+    L["ids"][:sample] = np.stack([rng.permutation(4) for _ in range(sample)]).astype(np.int32)
+    got, status = run_gpu(L)
+    assert status == 0, status
+    ids, wts = L["ids"][:sample], L["wts"][:sample]
+    r = oracle_impl.mx_moe_forward(L["a_bits"][:sample], ids, wts, L["w1p"][:4], L["w1s"][:4],
+                                   L["w2p"][:4], L["w2s"][:4], threads=oracle_impl.max_threads())
+    tol = forward_bound(r, ids, wts, k, n, topk, exact_gemm1=True)
+    err = np.abs(got[:sample] - r["out"])
+    bad = err > tol
+    assert not bad.any(), (int(bad.sum()), float(err.max()))
+
+
 def test_gpt_oss_like_layer(oracle_impl):
     """Hidden 2880, intermediate 2880, 4 experts, top-4 of 64 tokens."""
     check(oracle_impl, make_layer(64, 2880, 2880, 4, 4, seed=31))

@@ -130,6 +130,35 @@ def test_more_experts_than_the_compact_item_list(oracle_impl, big):
     run_case(oracle_impl, [int(r) for r in rows], 64, 64, seed=63 + big)
 
 
+def test_full_size_512_tokens_sampled_rows(oracle_impl):
+    """32 experts x 512 tokens against the gate+up weights [32, 5760, 2880] (the
+    benchmark's 512-token workload) on the GPU; the oracle recomputes 8 rows of
+    experts 0 and 31 (an output row depends on its own activation row only)."""
+    experts, rows_e, n, k, sample = 32, 512, 5760, 2880, 8
+    rows = [rows_e] * experts
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    total = int(offsets[-1])
+    rng = np.random.default_rng(71)
+    a_bits = inputs.bf16_normal_bits(rng, total * k).reshape(total, k)
+    w = inputs.mx_random(experts * n, k, 72, e_lo=118, e_hi=132, zero_fraction=True)
+    packed = w.packed.reshape(experts, n, k // 2)
+    scales = w.scales.reshape(experts, n, k // 32)
+    a_t = torch.from_numpy(a_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    out, status = fp4.fp4_mx_moe_gemm(a_t, torch.from_numpy(offsets).to(DEV), torch.from_numpy(packed).to(DEV),
+                                      torch.from_numpy(scales).to(DEV), rows_e)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got_all = out.float().cpu().numpy().astype(np.float64)
+    pick = [0, experts - 1]
+    sel = np.concatenate([np.arange(offsets[e], offsets[e] + sample) for e in pick])
+    sub_off = np.arange(len(pick) + 1, dtype=np.int64) * sample
+    exact, absdot = oracle_impl.mx_moe_gemm(a_bits[sel], sub_off, packed[pick], scales[pick],
+                                            threads=oracle_impl.max_threads())
+    err = np.abs(got_all[sel] - exact)
+    tol = tolerance(exact, absdot, k)
+    assert (err <= tol).all(), (int((err > tol).sum()), float(err.max()))
+
+
 def test_256_token_slabs_rows_beyond_capacity_flagged(oracle_impl):
     """The capacity check holds with 256-token slabs as well."""
     k, n = 64, 64
