@@ -204,7 +204,7 @@ FP4_EXPORT fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *exp
         return FP4_ERR_SHAPE;
     if (k % 32 != 0 || n % 32 != 0) return FP4_ERR_SHAPE;
     if (experts > 65535 || max_rows_per_expert > 65535ll * 128 || n > (1ll << 30) ||
-        k > (1ll << 30))
+        k > (1ll << 30) || total_rows > (1ll << 31) - 1024)  // 32-bit TMA row coordinates
         return FP4_ERR_SHAPE;
     if (experts == 0 || max_rows_per_expert == 0 || n == 0) return FP4_OK;
     if (a_bf16 == nullptr || expert_offsets == nullptr || w_packed == nullptr ||

@@ -210,7 +210,9 @@ fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_out, uint8_t
  *                        (as fp4_mx_unpack reads them); 16-byte aligned
  *   w_scales_e8m0        device, uint8[experts * n * k / 32]
  *   n, k                 output columns and reduction length, both multiples of 32
- *   total_rows           rows of a and out; an expert whose rows fall outside
+ *   total_rows           rows of a and out, below 2^31 - 1024 (the tensor-core
+ *                        loads address rows with 32-bit coordinates; else
+ *                        FP4_ERR_SHAPE); an expert whose rows fall outside
  *                        [0, total_rows) is not computed and status is set to
  *                        FP4_ERR_SHAPE (the offsets are checked on the device)
  *   out_bf16             device, uint16[total_rows * n], row-major; 16-byte aligned

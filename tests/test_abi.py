@@ -134,6 +134,8 @@ def test_moe_gemm_host_validation(lib):
     assert g(1, 8, 64, 48) == fp4.Status.ERR_SHAPE       # k % 32
     assert g(1, 8, 48, 64) == fp4.Status.ERR_SHAPE       # n % 32
     assert g(70000, 8, 64, 64) == fp4.Status.ERR_SHAPE   # experts > 65535
+    assert f(None, None, 1, 8, None, None, 64, 64, 2 ** 31 - 1000, None, None, None) \
+        == fp4.Status.ERR_SHAPE                           # rows past 32-bit TMA coordinates
     assert g(0, 8, 64, 64) == fp4.Status.OK
     assert g(1, 0, 64, 64) == fp4.Status.OK
     assert g(1, 8, 64, 64) == fp4.Status.ERR_NULL_PTR
