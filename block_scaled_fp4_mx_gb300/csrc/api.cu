@@ -239,7 +239,9 @@ bool moe_shape_ok(int64_t tokens, int64_t topk, int64_t experts, int64_t n, int6
     if (tokens < 0 || topk < 1 || topk > 1024 || experts < 1 || experts > 65535 || n < 32 ||
         k < 32 || n % 32 != 0 || k % 32 != 0 || n > (1ll << 20) || k > (1ll << 20))
         return false;
-    return tokens <= INT32_MAX / topk;  // slot and row indices are int32
+    // slot and row indices are int32, and the GEMMs' TMA row coordinates reach
+    // 320 rows past a slab's start
+    return tokens * topk <= (1ll << 31) - 1024;
 }
 
 }  // namespace

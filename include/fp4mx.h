@@ -248,7 +248,7 @@ fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *expert_offsets
  *                        contributes nothing and status is set to FP4_ERR_INDEX
  *   topk_weights         device, fp32[tokens * topk]
  *   tokens, topk         tokens >= 0 (0: nothing is launched), 1 <= topk <= 1024,
- *                        tokens * topk < 2^31
+ *                        tokens * topk <= 2^31 - 1024
  *   experts              1 .. 65535
  *   max_rows_per_expert  capacity of one expert (values above tokens * topk are
  *                        treated as tokens * topk); the slots of an expert that

@@ -185,6 +185,7 @@ def test_moe_forward_host_validation(lib):
     assert ws(16, 2, 4, 63, 64) == -1 and ws(16, 2, 4, 64, 48) == -1      # n, k % 32
     assert ws(16, 0, 4, 64, 64) == -1 and ws(16, 2, 0, 64, 64) == -1      # topk, experts
     assert ws(2 ** 30, 4, 4, 64, 64) == -1                                 # slots >= 2^31
+    assert ws(2 ** 31 - 1000, 1, 4, 64, 64) == -1                          # TMA row coordinates
     f = lib.fp4_mx_moe_forward
     base = 1 << 40
     tokens, topk, experts, n, k = 16, 2, 4, 64, 64
