@@ -156,12 +156,46 @@ def test_pages_zero_code_layer_is_exactly_zero():
 
 @pytest.mark.parametrize("tokens,k,n,experts,topk", [(1, 32, 32, 1, 1), (40, 128, 96, 5, 2),
                                                      (37, 64, 160, 3, 3), (130, 96, 64, 4, 1),
-                                                     (300, 128, 96, 3, 2), (700, 64, 224, 2, 1)])
+                                                     (300, 128, 96, 3, 2), (700, 64, 224, 2, 1),
+                                                     (400, 32, 32, 2, 1)])
 def test_small_layers(oracle_impl, tokens, k, n, experts, topk):
     """Single token and expert; n and k that are not multiples of the tiles; more
     than 128 tokens (256-token slabs: gate and up halves in one tile, N = 128 MMAs
-    for slabs with at most 128 live tokens, ragged 64-column tiles); topk 1 to 3."""
+    for slabs with at most 128 live tokens, ragged 64-column tiles, and n = 32: half
+    of one 64-column tile); topk 1 to 3."""
     check(oracle_impl, make_layer(tokens, k, n, experts, topk, seed=tokens + k + n))
+
+
+@pytest.mark.parametrize("topk", [6, 8, 9, 16])
+def test_wide_topk(oracle_impl, topk):
+    """Top-6 and top-8 take the combine's path that loads every slot's row vector
+    before the sum (8 slots at most); top-9 and top-16 its slot-by-slot loop."""
+    check(oracle_impl, make_layer(50, 64, 96, 24, topk, seed=71 + topk))
+
+
+def test_wide_topk_skips_bad_and_dropped_slots(oracle_impl):
+    """The slot-by-slot combine (top-12) skips a slot with a bad expert id, and the
+    slots of an expert over capacity, as the 8-slot path does."""
+    L = make_layer(30, 64, 64, 16, 12, seed=83)
+    ids = L["ids"]
+    for m in range(ids.shape[0]):  # expert 0 in every token, at slot 5
+        hit = np.flatnonzero(ids[m] == 0)
+        if hit.size:
+            ids[m, hit[0]], ids[m, 5] = ids[m, 5], ids[m, hit[0]]
+        else:
+            ids[m, 5] = 0
+    counts = np.bincount(ids.reshape(-1), minlength=16)
+    assert counts[0] == 30 and counts[1:].max() <= 29
+    ids[7, 2] = 16  # a bad id in a token that keeps its other slots
+    oracle_ids = ids.copy()
+    oracle_ids[oracle_ids == 0] = -1  # expert 0 holds 30 rows > capacity 29
+    got, status = run_gpu(L, max_rows=29)
+    assert status in (fp4.Status.ERR_SHAPE, fp4.Status.ERR_INDEX)
+    k, n = L["a_bits"].shape[1], L["w2p"].shape[2] * 2
+    r = oracle_impl.mx_moe_forward(L["a_bits"], oracle_ids, L["wts"], L["w1p"], L["w1s"], L["w2p"],
+                                   L["w2s"], threads=oracle_impl.max_threads())
+    tol = forward_bound(r, oracle_ids, L["wts"], k, n, 12, exact_gemm1=True)
+    assert (np.abs(got - r["out"]) <= tol).all()
 
 
 def test_extended_last_slabs(oracle_impl):
