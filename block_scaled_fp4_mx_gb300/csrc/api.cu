@@ -75,6 +75,10 @@ fp4_status check_pointers(const void *const *ptrs, int n) {
     return FP4_OK;
 }
 
+// Largest NVFP4 row (hidden) and paged-unpack page (page_elems), in codes: the row
+// and page kernels count a row's words and 128-word segments in 32 bits.
+constexpr int64_t kMaxRowCodes = (int64_t)1 << 31;
+
 constexpr int kMaxDevices = 64;
 constexpr int kSlots = 8;
 std::atomic<int> g_resident[kMaxDevices][kSlots];
@@ -138,6 +142,7 @@ FP4_EXPORT fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_id
     if (num_ids < 0 || vocab < 0 || hidden <= 0 || group_size <= 0) return FP4_ERR_SHAPE;
     if (hidden % group_size != 0) return FP4_ERR_GROUP;
     if (group_size != 16) return FP4_ERR_UNSUPPORTED;
+    if (hidden > kMaxRowCodes) return FP4_ERR_SHAPE;
     if (num_ids == 0) return FP4_OK;
     if (vocab == 0) return FP4_ERR_SHAPE;
     if (num_ids > INT64_MAX / 2 / hidden || vocab > INT64_MAX / hidden) return FP4_ERR_SHAPE;
@@ -349,7 +354,8 @@ FP4_EXPORT fp4_status fp4_mx_unpack_pages(const int64_t *page_ids, int64_t num_p
                                           int64_t page_elems, uint16_t *out_bf16,
                                           int32_t *err_flag, fp4_stream_t stream) {
     clear_error();
-    if (num_pages < 0 || pool_pages < 0 || page_elems <= 0 || page_elems % 32 != 0)
+    if (num_pages < 0 || pool_pages < 0 || page_elems <= 0 || page_elems % 32 != 0 ||
+        page_elems > kMaxRowCodes)
         return FP4_ERR_SHAPE;
     if (num_pages == 0) return FP4_OK;
     if (pool_pages == 0) return FP4_ERR_SHAPE;
@@ -389,6 +395,7 @@ FP4_EXPORT fp4_status fp4_nv_dequant(const uint8_t *weight, const uint8_t *block
     if (rows < 0 || hidden <= 0 || group_size <= 0) return FP4_ERR_SHAPE;
     if (hidden % group_size != 0) return FP4_ERR_GROUP;
     if (group_size != 16) return FP4_ERR_UNSUPPORTED;
+    if (hidden > kMaxRowCodes) return FP4_ERR_SHAPE;
     if (rows == 0) return FP4_OK;
     if (rows > INT64_MAX / 2 / hidden) return FP4_ERR_SHAPE;
     if (weight == nullptr || block_scale_e4m3 == nullptr || global_scale == nullptr ||
@@ -427,4 +434,4 @@ FP4_EXPORT const char *fp4_status_string(fp4_status status) {
 
 FP4_EXPORT const char *fp4_last_error(void) { return g_last_error; }
 
-FP4_EXPORT int fp4_abi_version(void) { return 107; }
+FP4_EXPORT int fp4_abi_version(void) { return 108; }

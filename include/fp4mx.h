@@ -120,7 +120,8 @@ fp4_status fp4_mx_unpack(const uint8_t *packed, const uint8_t *scales_e8m0, uint
  *                    synchronisation is needed and the call can be graph-captured)
  *   vocab            >= 1 when num_ids > 0
  *   hidden           > 0, hidden % group_size == 0 (else FP4_ERR_GROUP, the check
- *                    the pages' create_weights performs)
+ *                    the pages' create_weights performs), hidden <= 2^31 (else
+ *                    FP4_ERR_SHAPE: a row's word and segment counts are 32-bit)
  *   group_size       must be 16 (NVFP4); other positive values: FP4_ERR_UNSUPPORTED
  *   out_bf16         device, uint16[num_ids * hidden], row-major [num_ids, hidden]
  *   err_flag         device int32 or NULL. An id outside [0, vocab) never faults:
@@ -148,7 +149,8 @@ fp4_status fp4_nv_embedding_gather(const int64_t *ids, int64_t num_ids, const ui
  *   packed_pool       device, uint8[pool_pages * page_elems / 2], [pool_pages, page_elems/2]
  *   scales_pool_e8m0  device, uint8[pool_pages * page_elems / 32]
  *   pool_pages        >= 1 when num_pages > 0
- *   page_elems        codes per page, a positive multiple of 32 (else FP4_ERR_SHAPE)
+ *   page_elems        codes per page, a positive multiple of 32, at most 2^31 (else
+ *                     FP4_ERR_SHAPE: a page's word and segment counts are 32-bit)
  *   out_bf16          device, uint16[num_pages * page_elems], row-major
  *   err_flag          device int32 or NULL: a page id outside [0, pool_pages) gives a
  *                     +0.0 row and sets *err_flag to FP4_ERR_INDEX (never cleared)
@@ -341,7 +343,8 @@ fp4_status fp4_wait_selftest(int32_t mode, int32_t *status, fp4_stream_t stream)
  *   block_scale_e4m3 device, uint8[rows * hidden / 16] e4m3fn bits, [rows, hidden/16]
  *   global_scale     device, one fp32
  *   rows             >= 0 (0: nothing is launched)
- *   hidden           > 0, hidden % group_size == 0 (else FP4_ERR_GROUP)
+ *   hidden           > 0, hidden % group_size == 0 (else FP4_ERR_GROUP), hidden <= 2^31
+ *                    (else FP4_ERR_SHAPE)
  *   group_size       must be 16; other positive values: FP4_ERR_UNSUPPORTED
  *   out_bf16         device, uint16[rows * hidden], row-major [rows, hidden]
  *   stream           CUDA stream the kernel is enqueued on
@@ -361,7 +364,8 @@ const char *fp4_last_error(void);
  * fp4_mx_quantize and FP4_ERR_ALIGN, 103 adds fp4_mx_moe_gemm and FP4_ERR_TIMEOUT,
  * 104 adds fp4_mx_unpack_pages, 105 adds fp4_mx_moe_forward and
  * fp4_mx_moe_workspace_bytes, 106 adds fp4_mx_moe_forward_noalloc and
- * fp4_mx_moe_static_scratch_bytes, 107 adds fp4_wait_selftest. */
+ * fp4_mx_moe_static_scratch_bytes, 107 adds fp4_wait_selftest, 108 bounds hidden
+ * (NVFP4 gather and dequant) and page_elems (paged unpack) at 2^31. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

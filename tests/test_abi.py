@@ -56,7 +56,7 @@ def test_status_strings(lib):
     for code in range(1, 11):
         assert fp4.fp4_status_string(code) not in ("", "unknown status")
     assert fp4.fp4_status_string(99) == "unknown status"
-    assert lib.fp4_abi_version() == 107
+    assert lib.fp4_abi_version() == 108
 
 
 def test_mx_host_validation(lib):
@@ -85,6 +85,11 @@ def test_nv_host_validation(lib):
     assert f(*args(0, 10, 64, 16)) == fp4.Status.OK               # no ids: no launch
     assert f(*args(4, 0, 64, 16)) == fp4.Status.ERR_SHAPE         # ids but empty table
     assert f(*args(4, 10, 64, 16)) == fp4.Status.ERR_NULL_PTR
+    # rows longer than 2^31 codes are refused (32-bit word and segment counts), even
+    # when there are no ids; 2^31 itself passes the size checks
+    assert f(*args(4, 10, 2 ** 31 + 16, 16)) == fp4.Status.ERR_SHAPE
+    assert f(*args(0, 10, 2 ** 31 + 16, 16)) == fp4.Status.ERR_SHAPE
+    assert f(*args(1, 10, 2 ** 31, 16)) == fp4.Status.ERR_NULL_PTR
 
 
 def test_nv_dequant_host_validation(lib):
@@ -96,6 +101,8 @@ def test_nv_dequant_host_validation(lib):
     assert f(*args(4, 0, 16)) == fp4.Status.ERR_SHAPE
     assert f(*args(0, 64, 16)) == fp4.Status.OK
     assert f(*args(4, 64, 16)) == fp4.Status.ERR_NULL_PTR
+    assert f(*args(4, 2 ** 31 + 16, 16)) == fp4.Status.ERR_SHAPE
+    assert f(*args(1, 2 ** 31, 16)) == fp4.Status.ERR_NULL_PTR
 
 
 def test_mx_quantize_host_validation(lib):
@@ -154,6 +161,10 @@ def test_pages_host_validation(lib):
     assert g(0, 4, 64) == fp4.Status.OK
     assert g(2, 0, 64) == fp4.Status.ERR_SHAPE    # ids but no pool
     assert g(2, 4, 64) == fp4.Status.ERR_NULL_PTR
+    # pages longer than 2^31 codes are refused (32-bit word and segment counts)
+    assert g(2, 4, 2 ** 31 + 32) == fp4.Status.ERR_SHAPE
+    assert g(0, 4, 2 ** 31 + 32) == fp4.Status.ERR_SHAPE
+    assert g(1, 4, 2 ** 31) == fp4.Status.ERR_NULL_PTR
 
 
 def test_binding_refuses_cpu_tensors():
