@@ -209,7 +209,8 @@ FP4_EXPORT fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *exp
         return FP4_ERR_SHAPE;
     if (k % 32 != 0 || n % 32 != 0) return FP4_ERR_SHAPE;
     if (experts > 65535 || max_rows_per_expert > 65535ll * 128 || n > (1ll << 30) ||
-        k > (1ll << 30) || total_rows > (1ll << 31) - 1024)  // 32-bit TMA row coordinates
+        k > (1ll << 30) || total_rows > (1ll << 31) - 1024 ||  // 32-bit TMA row coordinates
+        experts * n > (1ll << 31) - 1024)                      // of activations and weights
         return FP4_ERR_SHAPE;
     if (experts == 0 || max_rows_per_expert == 0 || n == 0) return FP4_OK;
     if (a_bf16 == nullptr || expert_offsets == nullptr || w_packed == nullptr ||
@@ -245,8 +246,9 @@ bool moe_shape_ok(int64_t tokens, int64_t topk, int64_t experts, int64_t n, int6
         k < 32 || n % 32 != 0 || k % 32 != 0 || n > (1ll << 20) || k > (1ll << 20))
         return false;
     // slot and row indices are int32, and the GEMMs' TMA row coordinates reach
-    // 320 rows past a slab's start
-    return tokens * topk <= (1ll << 31) - 1024;
+    // 320 rows past a slab's start (activations) or a box past a tile (weights)
+    constexpr int64_t kMaxRows = (1ll << 31) - 1024;
+    return tokens * topk <= kMaxRows && experts * 2 * n <= kMaxRows && experts * k <= kMaxRows;
 }
 
 }  // namespace

@@ -211,7 +211,9 @@ fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_out, uint8_t
  *   w_packed             device, uint8[experts * n * k / 2]: expert e's [n, k/2] codes
  *                        (as fp4_mx_unpack reads them); 16-byte aligned
  *   w_scales_e8m0        device, uint8[experts * n * k / 32]
- *   n, k                 output columns and reduction length, both multiples of 32
+ *   n, k                 output columns and reduction length, both multiples of 32;
+ *                        experts * n <= 2^31 - 1024 (the weight loads, too, address
+ *                        rows with 32-bit coordinates; else FP4_ERR_SHAPE)
  *   total_rows           rows of a and out, below 2^31 - 1024 (the tensor-core
  *                        loads address rows with 32-bit coordinates; else
  *                        FP4_ERR_SHAPE); an expert whose rows fall outside
@@ -261,7 +263,9 @@ fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *expert_offsets
  *   w1_scales_e8m0       device, uint8[experts * 2n * k / 32]
  *   w2_packed            device, uint8[experts * k * n / 2]; 16-byte aligned
  *   w2_scales_e8m0       device, uint8[experts * k * n / 32]
- *   n, k                 intermediate and hidden sizes: multiples of 32, 32 .. 2^20
+ *   n, k                 intermediate and hidden sizes: multiples of 32, 32 .. 2^20,
+ *                        with experts * 2n and experts * k <= 2^31 - 1024 (weight rows
+ *                        of the two GEMMs, addressed with 32-bit coordinates)
  *   workspace            device scratch of workspace_bytes >= fp4_mx_moe_workspace_bytes(),
  *                        256-byte aligned; owned by the caller, overwritten by the call,
  *                        not read afterwards
@@ -365,7 +369,8 @@ const char *fp4_last_error(void);
  * 104 adds fp4_mx_unpack_pages, 105 adds fp4_mx_moe_forward and
  * fp4_mx_moe_workspace_bytes, 106 adds fp4_mx_moe_forward_noalloc and
  * fp4_mx_moe_static_scratch_bytes, 107 adds fp4_wait_selftest, 108 bounds hidden
- * (NVFP4 gather and dequant) and page_elems (paged unpack) at 2^31. */
+ * (NVFP4 gather and dequant) and page_elems (paged unpack) at 2^31 and the MoE
+ * weight rows (experts * n, experts * 2n, experts * k) at 2^31 - 1024. */
 int fp4_abi_version(void);
 
 #ifdef __cplusplus

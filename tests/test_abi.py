@@ -143,6 +143,8 @@ def test_moe_gemm_host_validation(lib):
     assert g(70000, 8, 64, 64) == fp4.Status.ERR_SHAPE   # experts > 65535
     assert f(None, None, 1, 8, None, None, 64, 64, 2 ** 31 - 1000, None, None, None) \
         == fp4.Status.ERR_SHAPE                           # rows past 32-bit TMA coordinates
+    assert g(32768, 8, 65536, 64) == fp4.Status.ERR_SHAPE  # weight rows experts * n = 2^31
+    assert g(32767, 8, 65536, 64) == fp4.Status.ERR_NULL_PTR  # 2^31 - 2^16: within the bound
     assert g(0, 8, 64, 64) == fp4.Status.OK
     assert g(1, 0, 64, 64) == fp4.Status.OK
     assert g(1, 8, 64, 64) == fp4.Status.ERR_NULL_PTR
@@ -197,6 +199,9 @@ def test_moe_forward_host_validation(lib):
     assert ws(16, 0, 4, 64, 64) == -1 and ws(16, 2, 0, 64, 64) == -1      # topk, experts
     assert ws(2 ** 30, 4, 4, 64, 64) == -1                                 # slots >= 2^31
     assert ws(2 ** 31 - 1000, 1, 4, 64, 64) == -1                          # TMA row coordinates
+    assert ws(16, 2, 2048, 2 ** 19, 64) == -1                              # experts * 2n = 2^31
+    assert ws(16, 2, 2048, 64, 2 ** 20) == -1                              # experts * k = 2^31
+    assert ws(16, 2, 2047, 2 ** 19, 2 ** 20) > 0                           # both just within
     f = lib.fp4_mx_moe_forward
     base = 1 << 40
     tokens, topk, experts, n, k = 16, 2, 4, 64, 64
