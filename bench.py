@@ -883,14 +883,15 @@ def run_e2e(args, d, dev, ops, step_elems):
 # CPU oracle timings
 # ---------------------------------------------------------------------------
 
-def cpu_rates(ops, seconds: float):
+def cpu_rates(ops, seconds: float, threads: int | None = None):
     """Oracle throughput (elements/s) per op kind, on leading units (rows or ids)
-    of the first op of that kind, sized to take about ``seconds`` each.
+    of the first op of that kind, sized to take about ``seconds`` each, on
+    ``threads`` host threads (default: all of them).
     Returns ({kind: (rate, units)}, description, threads)."""
     import oracle
 
     o = oracle.get()
-    threads = o.max_threads()
+    threads = o.max_threads() if threads is None else threads
     rates, desc = {}, []
     for kind in dict.fromkeys(op.kind for op in ops):
         op = next(p for p in ops if p.kind == kind)
@@ -914,13 +915,21 @@ def cpu_rates(ops, seconds: float):
 
 
 def cpu_baseline(ops, budget_s: float = 10.0) -> dict:
+    """The oracle on all host threads (the reported value) and, on a quarter of the
+    budget, on one thread."""
     kinds = list(dict.fromkeys(op.kind for op in ops))
-    rates, desc, threads = cpu_rates(ops, budget_s / max(1, len(kinds)))
-    t_step = sum(op.elems / rates[op.kind][0] for op in ops)
     total = sum(op.elems for op in ops)
-    return {"value": total / t_step, "unit": UNIT, "cores": threads, "kind": "oracle",
+
+    def combined(rates):
+        return total / sum(op.elems / rates[op.kind][0] for op in ops)
+
+    rates, desc, threads = cpu_rates(ops, budget_s / max(1, len(kinds)))
+    rates1, desc1, _ = cpu_rates(ops, budget_s / 4 / max(1, len(kinds)), threads=1)
+    return {"value": combined(rates), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": desc + "; rates combined in the step's element mix",
             "elements_per_s_by_kernel": {kind: rates[kind][0] for kind in kinds},
+            "single_thread": {"value": combined(rates1), "cores": 1, "sample": desc1,
+                              "elements_per_s_by_kernel": {kind: rates1[kind][0] for kind in kinds}},
             "cpu": _cpu_model()}
 
 
