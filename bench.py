@@ -483,7 +483,7 @@ class MoeForwardOp:
     silu(gate) * up, down GEMM, top-k weighted sum) on the MoE weights: 4,096 tokens,
     top-4 of 32 experts, hidden 2,880, intermediate 2,880."""
     kind, kernel = "mx_moe_forward", "mx_moe_forward (all kernels)"
-    launches = 6  # count, scan, scatter, gate/up GEMM, down GEMM, combine
+    launches = 5  # route (count + scan), scatter, gate/up GEMM, down GEMM, combine
 
     def __init__(self, w1, w2, tokens: int = 4096, topk: int = 4, seed: int = 9):
         from block_scaled_fp4_mx_gb300 import inputs

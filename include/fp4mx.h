@@ -3,7 +3,7 @@
  * (E2M1) data into bf16.
  *
  * The operations below; each is one CUDA kernel launch on the caller's stream,
- * except the MoE layer (one memset and six launches):
+ * except the MoE layer (one memset and five launches):
  *
  *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
  *                             a wrapping 16-bit integer add into the bf16 exponent

@@ -303,7 +303,7 @@ def test_equals_gemm_composition():
 
 
 def test_graph_capture_and_replay(oracle_impl):
-    """The layer (one memset and six launches on the caller's stream) can be captured
+    """The layer (one memset and five launches on the caller's stream) can be captured
     in a CUDA graph once and replayed for new activations, routing and weights of the
     top-k written into the captured buffers; each replay matches the oracle for its
     own inputs. 150 rows per expert on average: 256-token slabs."""
