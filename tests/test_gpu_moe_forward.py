@@ -349,3 +349,57 @@ def test_graph_capture_and_replay(oracle_impl):
                                        L["w2s"], threads=oracle_impl.max_threads())
         tol = forward_bound(r, L["ids"], L["wts"], k, n, topk, exact_gemm1=True)
         assert (np.abs(got - r["out"]) <= tol).all()
+
+
+def test_concurrent_host_threads(oracle_impl):
+    """Four host threads, each on its own CUDA stream, call the MXFP4 unpack, the
+    NVFP4 gather and the layer ten times each into outputs of their own: every result
+    equals the oracle's (unpack, gather) or the first single-threaded layer call's,
+    bit for bit. The layer is deterministic: the order of rows inside an expert's
+    segment changes no value."""
+    import threading
+    xm = inputs.mx_random(96, 2880, seed=101)
+    xn = inputs.nv_random(700, 2048, (128,), seed=102)
+    want_m = oracle_impl.mx_unpack(xm.packed, xm.scales).reshape(-1)
+    want_n = oracle_impl.nv_embedding_gather(xn.ids, xn.weight, xn.scales, xn.global_scale)[0].reshape(-1)
+    p, s = torch.from_numpy(xm.packed).to(DEV), torch.from_numpy(xm.scales).to(DEV)
+    ids, w = torch.from_numpy(xn.ids).to(DEV), torch.from_numpy(xn.weight).to(DEV)
+    sc = torch.from_numpy(xn.scales).to(DEV)
+    gs = torch.tensor([xn.global_scale], dtype=torch.float32, device=DEV)
+    L = make_layer(200, 128, 96, 6, 3, seed=103)
+    t = {key: torch.from_numpy(L[key]).to(DEV) for key in ("ids", "wts", "w1p", "w1s", "w2p", "w2s")}
+    a = torch.from_numpy(L["a_bits"].view(np.int16)).to(DEV).view(torch.bfloat16)
+
+    def layer():
+        return fp4.fp4_mx_moe_forward(a, t["ids"], t["wts"], t["w1p"], t["w1s"], t["w2p"], t["w2s"])
+
+    first, st0 = layer()
+    torch.cuda.synchronize()
+    assert int(st0.item()) == 0
+    want_l = first.view(torch.int16).cpu().numpy()
+    errors = []
+
+    def worker(i):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for r in range(10):
+                    om = fp4.fp4_mx_unpack(p, s)
+                    on = fp4.fp4_nv_embedding_gather(ids, w, sc, gs)
+                    ol, status = layer()
+                    stream.synchronize()
+                    if not np.array_equal(om.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1), want_m):
+                        errors.append(f"thread {i} round {r}: unpack")
+                    if not np.array_equal(on.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1), want_n):
+                        errors.append(f"thread {i} round {r}: gather")
+                    if int(status.item()) != 0 or not np.array_equal(ol.view(torch.int16).cpu().numpy(), want_l):
+                        errors.append(f"thread {i} round {r}: layer")
+        except Exception as exc:  # noqa: BLE001 -- reported below
+            errors.append(f"thread {i}: {exc!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors[:5]
