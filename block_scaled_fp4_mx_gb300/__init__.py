@@ -86,6 +86,14 @@ def _ptr(t):
     return ctypes_void(t.data_ptr()) if t is not None and t.numel() else ctypes_void(0)
 
 
+def _call(device, name: str, *args):
+    """Calls the C entry point ``name`` with ``device`` (the tensors' device) as the
+    current CUDA device, which the library's pointer checks and launches use."""
+    torch = _torch()
+    with torch.cuda.device(device):
+        return getattr(load(), name)(*args)
+
+
 def fp4_mx_unpack(packed, scales_e8m0, out=None, stream=None):
     """MXFP4 -> bf16. ``packed`` uint8 [..., k/2], ``scales_e8m0`` uint8 [..., k/32]
     with the same leading dimensions; returns (or fills ``out``) bf16 [..., k].
@@ -108,8 +116,8 @@ def fp4_mx_unpack(packed, scales_e8m0, out=None, stream=None):
         _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
         if tuple(out.shape) != shape:
             raise ValueError(f"out must have shape {shape}")
-    code = load().fp4_mx_unpack(_ptr(packed), _ptr(scales_e8m0), _ptr(out), rows, k,
-                                _stream_handle(stream, packed.device))
+    code = _call(packed.device, "fp4_mx_unpack", _ptr(packed), _ptr(scales_e8m0), _ptr(out),
+                 rows, k, _stream_handle(stream, packed.device))
     if code != Status.OK:
         raise Fp4Error("fp4_mx_unpack", code)
     return out
@@ -148,7 +156,8 @@ def fp4_nv_embedding_gather(ids, weight, block_scale, global_scale, group_size: 
             raise ValueError(f"out must have shape {shape}")
     if err_flag is not None:
         _check_cuda(err_flag, "err_flag", (torch.int32,))
-    code = load().fp4_nv_embedding_gather(
+    code = _call(
+        weight.device, "fp4_nv_embedding_gather",
         _ptr(ids), ids.numel(), _ptr(weight), _ptr(block_scale), _ptr(global_scale), vocab,
         hidden, int(group_size), _ptr(out), _ptr(err_flag),
         _stream_handle(stream, weight.device))
@@ -183,9 +192,9 @@ def fp4_nv_dequant(weight, block_scale, global_scale, group_size: int = 16, out=
         _check_cuda(out, "out", (torch.bfloat16, torch.int16, torch.uint16))
         if tuple(out.shape) != (rows, hidden):
             raise ValueError(f"out must have shape {(rows, hidden)}")
-    code = load().fp4_nv_dequant(_ptr(weight), _ptr(block_scale), _ptr(global_scale), rows,
-                                 hidden, int(group_size), _ptr(out),
-                                 _stream_handle(stream, weight.device))
+    code = _call(weight.device, "fp4_nv_dequant", _ptr(weight), _ptr(block_scale),
+                 _ptr(global_scale), rows, hidden, int(group_size), _ptr(out),
+                 _stream_handle(stream, weight.device))
     if code != Status.OK:
         raise Fp4Error("fp4_nv_dequant", code)
     return out
@@ -210,8 +219,8 @@ def fp4_mx_quantize(x, packed_out=None, scales_out=None, stream=None):
     _check_cuda(scales_out, "scales_out", (torch.uint8,))
     if tuple(packed_out.shape) != p_shape or tuple(scales_out.shape) != s_shape:
         raise ValueError(f"outputs must have shapes {p_shape} and {s_shape}")
-    code = load().fp4_mx_quantize(_ptr(x), _ptr(packed_out), _ptr(scales_out), rows, k,
-                                  _stream_handle(stream, x.device))
+    code = _call(x.device, "fp4_mx_quantize", _ptr(x), _ptr(packed_out), _ptr(scales_out), rows,
+                 k, _stream_handle(stream, x.device))
     if code != Status.OK:
         raise Fp4Error("fp4_mx_quantize", code)
     return packed_out, scales_out
@@ -246,9 +255,9 @@ def fp4_mx_moe_gemm(a, expert_offsets, w_packed, w_scales, max_rows_per_expert: 
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=a.device)
     _check_cuda(status, "status", (torch.int32,))
-    code = load().fp4_mx_moe_gemm(_ptr(a), _ptr(expert_offsets), experts, int(max_rows_per_expert),
-                                  _ptr(w_packed), _ptr(w_scales), n, k, a.shape[0], _ptr(out),
-                                  _ptr(status), _stream_handle(stream, a.device))
+    code = _call(a.device, "fp4_mx_moe_gemm", _ptr(a), _ptr(expert_offsets), experts,
+                 int(max_rows_per_expert), _ptr(w_packed), _ptr(w_scales), n, k, a.shape[0],
+                 _ptr(out), _ptr(status), _stream_handle(stream, a.device))
     if code != Status.OK:
         raise Fp4Error("fp4_mx_moe_gemm", code)
     return out, status
@@ -304,7 +313,8 @@ def fp4_mx_moe_forward(a, topk_ids, topk_weights, w1_packed, w1_scales, w2_packe
         status = torch.zeros(1, dtype=torch.int32, device=a.device)
     _check_cuda(status, "status", (torch.int32,))
     max_rows = tokens if max_rows_per_expert is None else int(max_rows_per_expert)
-    code = load().fp4_mx_moe_forward(
+    code = _call(
+        a.device, "fp4_mx_moe_forward",
         _ptr(a), _ptr(topk_ids), _ptr(topk_weights), tokens, topk, experts, max_rows,
         _ptr(w1_packed), _ptr(w1_scales), _ptr(w2_packed), _ptr(w2_scales), n, k,
         _ptr(workspace), workspace.numel(), _ptr(out), _ptr(status),
@@ -355,7 +365,8 @@ def fp4_mx_moe_forward_noalloc(a, topk_ids, topk_weights, w1_packed, w1_scales, 
         status = torch.zeros(1, dtype=torch.int32, device=a.device)
     _check_cuda(status, "status", (torch.int32,))
     max_rows = tokens if max_rows_per_expert is None else int(max_rows_per_expert)
-    code = load().fp4_mx_moe_forward_noalloc(
+    code = _call(
+        a.device, "fp4_mx_moe_forward_noalloc",
         _ptr(a), _ptr(topk_ids), _ptr(topk_weights), tokens, topk, experts, max_rows,
         _ptr(w1_packed), _ptr(w1_scales), _ptr(w2_packed), _ptr(w2_scales), n, k, _ptr(out),
         _ptr(status), _stream_handle(stream, a.device))
@@ -374,7 +385,8 @@ def fp4_wait_selftest(mode, status=None, device="cuda", stream=None):
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=device)
     _check_cuda(status, "status", (torch.int32,))
-    code = load().fp4_wait_selftest(int(mode), _ptr(status), _stream_handle(stream, status.device))
+    code = _call(status.device, "fp4_wait_selftest", int(mode), _ptr(status),
+                 _stream_handle(stream, status.device))
     if code != Status.OK:
         raise Fp4Error("fp4_wait_selftest", code)
     return status
@@ -406,9 +418,9 @@ def fp4_mx_unpack_pages(page_ids, packed_pool, scales_pool, out=None, err_flag=N
             raise ValueError(f"out must have shape {shape}")
     if err_flag is not None:
         _check_cuda(err_flag, "err_flag", (torch.int32,))
-    code = load().fp4_mx_unpack_pages(_ptr(page_ids), page_ids.numel(), _ptr(packed_pool),
-                                      _ptr(scales_pool), pool_pages, page_elems, _ptr(out),
-                                      _ptr(err_flag), _stream_handle(stream, packed_pool.device))
+    code = _call(packed_pool.device, "fp4_mx_unpack_pages", _ptr(page_ids), page_ids.numel(),
+                 _ptr(packed_pool), _ptr(scales_pool), pool_pages, page_elems, _ptr(out),
+                 _ptr(err_flag), _stream_handle(stream, packed_pool.device))
     if code != Status.OK:
         raise Fp4Error("fp4_mx_unpack_pages", code)
     return out
