@@ -744,6 +744,7 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
     if (err != cudaSuccess) return err;
     const int64_t items = experts * ((max_rows + C::kTok - 1) / C::kTok) *
                           ((n_out + C::kTileCols - 1) / C::kTileCols);
+    if (items == 0) return cudaSuccess;  // no expert may hold a row (capacity 0): no work
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(items < sms ? items : sms);

@@ -271,6 +271,15 @@ def test_expert_over_capacity_is_dropped_and_flagged(oracle_impl):
     check(oracle_impl, L, max_rows=10, expect_status=fp4.Status.ERR_SHAPE, oracle_ids=oracle_ids)
 
 
+def test_zero_capacity_drops_every_slot():
+    """max_rows_per_expert = 0: every expert with a slot is over capacity, so the
+    layer launches no GEMM work, writes zeros and reports FP4_ERR_SHAPE."""
+    L = make_layer(24, 64, 64, 3, 2, seed=111)
+    got, status = run_gpu(L, max_rows=0)
+    assert status == fp4.Status.ERR_SHAPE
+    assert (got == 0).all()
+
+
 def test_equals_gemm_composition():
     """With top-1 routing and weight 1 the layer is the gate/up GEMM, the activation
     and the down GEMM of the standalone entry point, bit for bit in the down GEMM's
