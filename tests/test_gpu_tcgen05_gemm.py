@@ -171,6 +171,35 @@ def test_256_token_slabs_rows_beyond_capacity_flagged(oracle_impl):
     assert int(status.item()) == fp4.Status.ERR_SHAPE
 
 
+@pytest.mark.parametrize("experts", [3, 1030])
+def test_inconsistent_offsets_flagged(oracle_impl, experts):
+    """Offsets that run past total_rows (expert 1) or decrease (expert 2): those
+    experts are not computed, their rows of the output keep what was there, the
+    consistent expert 0 is computed, and the status word says FP4_ERR_SHAPE. Three
+    experts walk the compact item list, 1,030 the dense one."""
+    k, n, total = 64, 64, 60
+    offsets = np.full(experts + 1, total, dtype=np.int64)
+    offsets[:4] = [0, 20, 80, 60]  # expert 0: rows 0..19; 1: 20..79 (past 60); 2: 80..60
+    rng = np.random.default_rng(71)
+    a_bits = inputs.bf16_normal_bits(rng, total * k).reshape(total, k)
+    w = inputs.mx_random(experts * n, k, seed=72, e_lo=118, e_hi=132)
+    packed, scales = w.packed.reshape(experts, n, k // 2), w.scales.reshape(experts, n, k // 32)
+    canary = 0x7FC1
+    out = torch.full((total, n), canary, dtype=torch.int16, device=DEV)
+    _, status = fp4.fp4_mx_moe_gemm(
+        torch.from_numpy(a_bits.view(np.int16)).to(DEV).view(torch.bfloat16),
+        torch.from_numpy(offsets).to(DEV), torch.from_numpy(packed).to(DEV),
+        torch.from_numpy(scales).to(DEV), 64, out=out)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fp4.Status.ERR_SHAPE
+    got = out.cpu().numpy()
+    assert (got[20:] == canary).all()
+    exact, absdot = oracle_impl.mx_moe_gemm(a_bits[:20], np.array([0, 20], dtype=np.int64),
+                                            packed[:1], scales[:1])
+    first = out[:20].view(torch.bfloat16).float().cpu().numpy().astype(np.float64)
+    assert (np.abs(first - exact) <= tolerance(exact, absdot, k)).all()
+
+
 def test_large_k(oracle_impl):
     """A long reduction: k = 4160, 65 slices of 64."""
     run_case(oracle_impl, [40, 130], 160, 4096 + 64, seed=11)
