@@ -58,7 +58,7 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
                                   uint16_t *out, int32_t *status, cudaStream_t stream);
 
 // The MoE layer's static device scratch (fp4_mx_moe_forward_noalloc): its size,
-// and its address on the current device (looked up once per device).
+// and its address in the current context (looked up on every call).
 uint64_t moe_static_scratch_bytes();
 cudaError_t moe_static_scratch(void **address);
 

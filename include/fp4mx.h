@@ -291,17 +291,30 @@ int64_t fp4_mx_moe_workspace_bytes(int64_t tokens, int64_t topk, int64_t experts
 
 /*
  * fp4_mx_moe_forward_noalloc -- fp4_mx_moe_forward with the library's own static
- * scratch instead of a caller workspace (no cudaMalloc anywhere on the path).
+ * scratch instead of a caller workspace. The paper has no counterpart: this entry
+ * point exists for callers that cannot call cudaMalloc -- code running inside a
+ * host application that owns all device memory and hands out no allocator, code
+ * on a path where a device allocation (which may synchronise the device) is not
+ * allowed, or code that must not change the process's memory footprint per call.
  *
  * Same arguments, semantics and errors as fp4_mx_moe_forward (above) minus the
- * workspace. The scratch is a static __device__ array of
- * fp4_mx_moe_static_scratch_bytes() bytes per device, in a module of its own
- * that the driver loads (and zero-fills) the first time it is used; its address
- * is looked up once per device. A layer whose workspace would exceed it is
- * rejected with FP4_ERR_SHAPE before anything is launched (the reason is in
- * fp4_last_error()). The area is shared by every call on a device: calls must be
- * ordered (one stream, or events between streams); two overlapping calls would
- * overwrite each other's scratch. Thread-safe on the host.
+ * workspace; nothing on this path calls cudaMalloc, cudaFree or an allocating
+ * library routine. The scratch is a static __device__ array of
+ * fp4_mx_moe_static_scratch_bytes() bytes (288 MiB: the 4,096-token, top-4,
+ * 2880 x 2880 layer fits) in a module of its own. Under lazy module loading
+ * (CUDA_MODULE_LOADING=LAZY, the CUDA 12+ default) the driver loads that module,
+ * and reserves and zero-fills the array, on the first call on a device; make that
+ * first call before any stream capture begins. Under eager loading every process
+ * that loads this library reserves the 288 MiB on every device it uses, whether
+ * or not it ever calls this function. Every GPU that loads the module holds the
+ * array until the process exits. The array's address is looked up on every call
+ * (a host-side lookup), so it follows the current context, also after a reset.
+ * A layer whose workspace would exceed the array is rejected with FP4_ERR_SHAPE
+ * before anything is launched (the reason is in fp4_last_error()). Each call
+ * clears the counters it needs at zero itself. Every call on a device shares the
+ * one array and finds the previous call's contents in it: calls must be ordered
+ * (one stream, or events between streams); two calls that overlap on the GPU race
+ * and overwrite each other's scratch. Thread-safe on the host.
  */
 fp4_status fp4_mx_moe_forward_noalloc(const uint16_t *a_bf16, const int32_t *topk_ids,
                                       const float *topk_weights, int64_t tokens, int64_t topk,

@@ -1,11 +1,17 @@
 """fp4_mx_moe_forward_noalloc: the MoE layer on the library's static device scratch.
 
+This entry point serves callers that cannot allocate device memory themselves (a
+host application that owns all of it, or a path where an allocation must not
+happen); the file is named so that pytest collects it after the other test
+files, but every test here also passes alone, first or last in a process.
+
 Host side (no GPU): the entry points are exported, the scratch size is reported,
 and a layer that needs more scratch than the static area is rejected before any
 CUDA call. GPU: the result equals fp4_mx_moe_forward with a caller workspace bit
-for bit, repeated calls leave the device's free memory unchanged (nothing is
-allocated), the area is reused across layer sizes, and an oversized layer
-launches nothing.
+for bit on two calls in a row, also for a layer whose scratch reaches to within
+3 KiB of the end of the area; once the area is loaded, repeated calls leave the
+device's free memory unchanged (nothing is allocated); the area is reused across
+layer sizes; an oversized layer launches nothing.
 """
 import numpy as np
 import pytest
@@ -61,6 +67,9 @@ def test_noalloc_equals_workspace_forward_and_allocates_nothing():
         assert torch.equal(ref.view(torch.int16), got.view(torch.int16))
     out = torch.empty_like(big[0])
     status = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    # one call of exactly the measured form first: whatever loads on first use
+    # (the scratch module, the binding's own state) is in place before the reading
+    fp4.fp4_mx_moe_forward_noalloc(*big, out=out, status=status)
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     for _ in range(5):
@@ -68,6 +77,26 @@ def test_noalloc_equals_workspace_forward_and_allocates_nothing():
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, (free0, free1)
+    assert int(status.item()) == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_layer_filling_the_area():
+    """8,736 tokens, top-2 of 2 experts, 2880 x 2880: the scratch ends 3,072 bytes
+    before the end of the static area, so its last bytes are written and read."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tokens, k, n, experts, topk = 8736, 2880, 2880, 2, 2
+    need = fp4.fp4_mx_moe_workspace_bytes(tokens, topk, experts, n, k)
+    cap = fp4.fp4_mx_moe_static_scratch_bytes()
+    assert 0 <= cap - need <= 4096, (need, cap)
+    args = _layer(tokens, k, n, experts, topk, seed=11)
+    for _ in range(2):
+        ref, st0 = fp4.fp4_mx_moe_forward(*args)
+        got, st1 = fp4.fp4_mx_moe_forward_noalloc(*args)
+        torch.cuda.synchronize()
+        assert int(st0.item()) == 0 and int(st1.item()) == 0
+        assert torch.equal(ref.view(torch.int16), got.view(torch.int16))
 
 
 @pytest.mark.gpu
