@@ -1,13 +1,18 @@
 #!/usr/bin/env python
 """Throughput of the FP4 (E2M1) block-scaled decode path on one GB300 per rank.
 
-One step = one pass of the whole path over one batch of synthetic input:
-MXFP4 unpack of an MoE expert stack (gate+up [32, 5760, 2880] and down
-[32, 2880, 2880] codes; two fp4_mx_unpack launches) plus an NVFP4 embedding
-gather-dequant (vocab 200,000 x hidden 8,192, 16,384 Zipf(1.1) ids as [64, 256];
-one fp4_nv_embedding_gather launch). ``--workload`` picks one of the other named
-workloads instead (one entry point per step, e.g. ``nv_dequant_200k``: fp4_nv_dequant
-of the whole 200k x 8,192 table).
+One step = one pass of the whole path over the three large workloads: MXFP4
+unpack of an MoE expert stack (gate+up [32, 5760, 2880] and down [32, 2880, 2880]
+codes; two fp4_mx_unpack launches), an NVFP4 embedding gather-dequant (vocab
+200,000 x hidden 8,192, 16,384 Zipf(1.1) ids as [64, 256]; one
+fp4_nv_embedding_gather launch) and the MXFP4 stress stream (2^30 packed bytes,
+30% zero codes, exponents from {0, 107, 127, 137, 255}; one fp4_mx_unpack
+launch). The two small parity workloads (the exhaustive 256 x 256 unpack and the
+32k-vocabulary gather) are launch-bound; they are timed in the same run outside
+the step, and every workload is also timed alone (its launches back to back).
+``--workload`` picks one of the other named workloads instead (one entry point
+per step, e.g. ``nv_dequant_200k``: fp4_nv_dequant of the whole 200k x 8,192
+table).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -430,6 +435,7 @@ class MoeGemmOp:
         self.bytes = w.packed.size + w.scales.size + 2 * t * self.k + self.out_bytes
         self.min_bytes = self.bytes
         self.units, self.elems_per_unit = self.experts, self.n * self.k
+        self.label = f"mx_moe_gemm_{rows_per_expert}_tokens_per_expert_{self.n}x{self.k}"
 
     def to_device(self, torch, dev):
         self.a = torch.from_numpy(self.a_bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -505,6 +511,7 @@ class MoeForwardOp:
                       + 2 * tokens * self.k + 8 * slots + self.out_bytes)
         self.min_bytes = self.bytes
         self.units, self.elems_per_unit = self.experts, self.elems // self.experts
+        self.label = f"mx_moe_forward_{tokens}_tokens_top{topk}"
 
     def to_device(self, torch, dev):
         import block_scaled_fp4_mx_gb300 as fp4
@@ -591,7 +598,8 @@ def load_workload(name: str):
     """The ops of one step of the named workload, in launch order."""
     from block_scaled_fp4_mx_gb300 import inputs
     if name == "step":
-        return [MxOp(x) for x in inputs.mx_moe()] + [NvGatherOp(inputs.nv_embedding_200k())]
+        return ([MxOp(x) for x in inputs.mx_moe()] + [NvGatherOp(inputs.nv_embedding_200k())]
+                + [MxOp(inputs.mx_stress())])
     table = {
         "mx_moe": lambda: [MxOp(x) for x in inputs.mx_moe()],
         "mx_stress": lambda: [MxOp(inputs.mx_stress())],
@@ -609,10 +617,20 @@ def load_workload(name: str):
     return table[name]()
 
 
+def side_workload(name: str):
+    """Small workloads timed in the same run outside the step (latency figures):
+    the exhaustive 256 x 256 MXFP4 unpack and the 32k-vocabulary NVFP4 gather."""
+    from block_scaled_fp4_mx_gb300 import inputs
+    if name == "step":
+        return [MxOp(inputs.mx_exhaustive()), NvGatherOp(inputs.nv_embedding_32k())]
+    return []
+
+
 def workload_label(name: str) -> str:
     if name == "step":
         return ("mx_moe_unpack_32x(5760+2880)x2880 + "
-                "nv_embedding_gather_200000x8192_zipf1.1_ids64x256")
+                "nv_embedding_gather_200000x8192_zipf1.1_ids64x256 + "
+                "mx_stress_unpack_2^31_codes")
     return name
 
 
@@ -666,6 +684,46 @@ def ncu_traffic(kind: str, elements_per_launch: float):
 # our arm
 # ---------------------------------------------------------------------------
 
+def op_label(op) -> str:
+    """Name of the workload an op runs on (the input's name)."""
+    if hasattr(op, "label"):
+        return op.label
+    for attr in ("x", "w", "kv"):
+        v = getattr(op, attr, None)
+        if v is not None and hasattr(v, "name"):
+            return v.name
+    return op.kind
+
+
+def per_launch_record(op, launch_s: float, peak: float, tensor_peak: float) -> dict:
+    """Throughput figures of one launch of ``op`` that took ``launch_s`` seconds."""
+    rec = {"avg_launch_us": launch_s * 1e6, "elements": op.elems,
+           "elements_per_s": op.elems / launch_s, "algorithmic_bytes": op.bytes,
+           "gbs": op.bytes / launch_s / 1e9, "frac_of_peak": op.bytes / launch_s / 1e9 / peak}
+    if op.min_bytes != op.bytes:
+        rec["distinct_row_bytes"] = op.min_bytes
+        rec["gbs_distinct_rows"] = op.min_bytes / launch_s / 1e9
+        rec["frac_of_peak_distinct_rows"] = rec["gbs_distinct_rows"] / peak
+    if getattr(op, "flops", 0.0):
+        rec["tflops"] = op.flops / launch_s / 1e12
+        rec["frac_of_tensor_peak"] = rec["tflops"] / tensor_peak
+    return rec
+
+
+def time_alone(torch, fp4, op, stream, launches: int) -> float:
+    """Mean seconds per launch of ``op`` run back to back (after 3 warm-up launches)."""
+    for _ in range(3):
+        op.launch(fp4, stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(launches):
+        op.launch(fp4, stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / launches
+
+
 def run_ours(args, d: Dist):
     import torch
 
@@ -676,7 +734,8 @@ def run_ours(args, d: Dist):
     d.init("nccl")
     fp4.load()
     ops = load_workload(args.workload)
-    for op in ops:
+    side = [] if args.no_side else side_workload(args.workload)
+    for op in ops + side:
         op.to_device(torch, dev)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
@@ -719,15 +778,35 @@ def run_ours(args, d: Dist):
     peak, peak_kind = measured_peak()
     tensor_peak, tensor_kind = measured_tensor_peak()
 
-    # per kernel kind: summed bytes and durations of its launches
+    # per workload: its launch inside the step, and the same launch run back to back
+    op_ms = [sum(ev[i][0].elapsed_time(ev[i][1]) for ev in events) for i in range(len(ops))]
+    configs = []
+    for i, op in enumerate(ops):
+        rec = {"workload": op_label(op), "kernel": op.kernel, "in_step": True,
+               **per_launch_record(op, op_ms[i] / 1e3 / k, peak, tensor_peak)}
+        configs.append(rec)
+    for op in side:
+        configs.append({"workload": op_label(op), "kernel": op.kernel, "in_step": False})
+    if not args.no_alone:
+        for rec, op in zip(configs, ops + side):
+            launches = args.alone_launches if op.bytes > 64e6 else 10 * args.alone_launches
+            alone = per_launch_record(op, time_alone(torch, fp4, op, stream, launches), peak,
+                                      tensor_peak)
+            if rec["in_step"]:
+                rec["alone"] = {key: alone[key] for key in alone
+                                if key not in ("elements", "algorithmic_bytes", "distinct_row_bytes")}
+                rec["alone"]["launches"] = launches
+            else:
+                rec.update(alone, launches_timed=launches)
+
+    # per kernel kind: summed bytes and durations of its launches inside the step
     kernels = {}
     for i, op in enumerate(ops):
-        ms = sum(ev[i][0].elapsed_time(ev[i][1]) for ev in events)
         kk = kernels.setdefault(op.kind, {"kernel": op.kernel, "launches_per_step": 0, "ms": 0.0,
                                           "elements": 0, "bytes": 0, "min_bytes": 0, "flops": 0.0})
         kk["flops"] += getattr(op, "flops", 0.0)
         kk["launches_per_step"] += 1
-        kk["ms"] += ms
+        kk["ms"] += op_ms[i]
         kk["elements"] += op.elems
         kk["bytes"] += op.bytes
         kk["min_bytes"] += op.min_bytes
@@ -787,7 +866,11 @@ def run_ours(args, d: Dist):
     e2e = None if args.no_e2e else run_e2e(args, d, dev, ops, step_elems)
     cpu = None
     if d.rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(ops, budget_s=args.cpu_budget)
+        cpu = cpu_baseline(ops, side, budget_s=args.cpu_budget)
+        for rec in configs:
+            oc = cpu["by_workload"].get(rec["workload"])
+            if oc and "elements_per_s" in rec:
+                rec["oracle"] = oc
 
     out_bytes = sum(getattr(op, "out_bytes", 2 * op.elems) for op in ops)  # bf16 outputs by default
     in_bytes = step_bytes - out_bytes
@@ -806,8 +889,8 @@ def run_ours(args, d: Dist):
                    if step_bytes > 4 * 129e6 else "no flush: working set smaller than L2",
                    "parallelism": f"replicas x{d.world}"},
         "hbm_gbs_algorithmic": alg_gbs, "pct_of_peak_hbm": 100.0 * alg_gbs / peak,
-        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-        **({"comparison": comparison} if comparison else {}),
+        "roofline": roofline, "kernels": kernels, "configs": configs, "cpu_baseline": cpu,
+        "e2e": e2e, **({"comparison": comparison} if comparison else {}),
         "gpu_launches": sum(getattr(op, "launches", 1) for op in ops) * k,
         "clocks": sampler.summary(t0, t1),
         "device": torch.cuda.get_device_name(dev),
@@ -884,17 +967,17 @@ def run_e2e(args, d, dev, ops, step_elems):
 # ---------------------------------------------------------------------------
 
 def cpu_rates(ops, seconds: float, threads: int | None = None):
-    """Oracle throughput (elements/s) per op kind, on leading units (rows or ids)
-    of the first op of that kind, sized to take about ``seconds`` each, on
-    ``threads`` host threads (default: all of them).
-    Returns ({kind: (rate, units)}, description, threads)."""
+    """Oracle throughput (elements/s) per workload, on leading units (rows or ids)
+    of that workload's input, sized to take about ``seconds`` each, on ``threads``
+    host threads (default: all of them). Returns ({workload: (rate, units)},
+    description, threads)."""
     import oracle
 
     o = oracle.get()
     threads = o.max_threads() if threads is None else threads
     rates, desc = {}, []
-    for kind in dict.fromkeys(op.kind for op in ops):
-        op = next(p for p in ops if p.kind == kind)
+    for op in ops:
+        label = op_label(op)
         n = max(1, min(op.units, getattr(op, "cpu_start_units", 16)))
         while True:
             t = time.perf_counter()
@@ -909,27 +992,35 @@ def cpu_rates(ops, seconds: float, threads: int | None = None):
             op.oracle_units(o, n, threads)
             total += time.perf_counter() - t
             reps += 1
-        rates[kind] = (n * op.elems_per_unit * reps / total, n)
-        desc.append(f"{kind}: first {n} {op.sample_name()} ({n * op.elems_per_unit} codes) x{reps}")
+        rates[label] = (n * op.elems_per_unit * reps / total, n)
+        desc.append(f"{label}: first {n} {op.sample_name()} ({n * op.elems_per_unit} codes) x{reps}")
     return rates, "; ".join(desc), threads
 
 
-def cpu_baseline(ops, budget_s: float = 10.0) -> dict:
+def cpu_baseline(ops, side=(), budget_s: float = 12.0) -> dict:
     """The oracle on all host threads (the reported value) and, on a quarter of the
-    budget, on one thread."""
-    kinds = list(dict.fromkeys(op.kind for op in ops))
+    budget, on one thread; per workload, the rate on a leading sample and the time
+    the whole workload would take at that rate."""
+    everything = list(ops) + list(side)
     total = sum(op.elems for op in ops)
 
     def combined(rates):
-        return total / sum(op.elems / rates[op.kind][0] for op in ops)
+        return total / sum(op.elems / rates[op_label(op)][0] for op in ops)
 
-    rates, desc, threads = cpu_rates(ops, budget_s / max(1, len(kinds)))
-    rates1, desc1, _ = cpu_rates(ops, budget_s / 4 / max(1, len(kinds)), threads=1)
+    rates, desc, threads = cpu_rates(everything, budget_s / max(1, len(everything)))
+    rates1, desc1, _ = cpu_rates(everything, budget_s / 4 / max(1, len(everything)), threads=1)
+    by_workload = {}
+    for op in everything:
+        label = op_label(op)
+        by_workload[label] = {
+            "elements_per_s": rates[label][0], "elements_per_s_1_thread": rates1[label][0],
+            "seconds_whole_workload": op.elems / rates[label][0],
+            "seconds_whole_workload_1_thread": op.elems / rates1[label][0],
+            "sample_units": rates[label][1], "whole": rates[label][1] == op.units}
     return {"value": combined(rates), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": desc + "; rates combined in the step's element mix",
-            "elements_per_s_by_kernel": {kind: rates[kind][0] for kind in kinds},
-            "single_thread": {"value": combined(rates1), "cores": 1, "sample": desc1,
-                              "elements_per_s_by_kernel": {kind: rates1[kind][0] for kind in kinds}},
+            "by_workload": by_workload,
+            "single_thread": {"value": combined(rates1), "cores": 1, "sample": desc1},
             "cpu": _cpu_model()}
 
 
@@ -952,15 +1043,14 @@ def run_reference(args, d: Dist):
 
     oracle.build()
     ops = load_workload(args.workload)
-    kinds = list(dict.fromkeys(op.kind for op in ops))
     per_step = max(0.5, min(20.0, args.reference_budget / max(1, args.steps + args.warmup)))
-    rates, desc, threads = cpu_rates(ops, per_step / len(kinds))
+    rates, desc, threads = cpu_rates(ops, per_step / len(ops))
     o = oracle.get()
-    # each step: one leading slice per op kind, sized to about per_step / kinds seconds
+    # each step: one leading slice of every workload, sized to about per_step / ops seconds
     plan = []
-    for kind in kinds:
-        op = next(p for p in ops if p.kind == kind)
-        n = max(1, min(op.units, int(rates[kind][0] * per_step / len(kinds) / op.elems_per_unit)))
+    for op in ops:
+        rate = rates[op_label(op)][0]
+        n = max(1, min(op.units, int(rate * per_step / len(ops) / op.elems_per_unit)))
         plan.append((op, n))
     sample_elems = sum(n * op.elems_per_unit for op, n in plan)
     times = []
@@ -1010,7 +1100,13 @@ def main(argv=None):
                     help="row chunks per tensor in the e2e leg (half as many for a gather)")
     ap.add_argument("--e2e-streams", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=10.0,
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the small parity workloads timed outside the step")
+    ap.add_argument("--no-alone", action="store_true",
+                    help="skip timing each workload alone (launches back to back)")
+    ap.add_argument("--alone-launches", type=int, default=20,
+                    help="launches per large workload in the alone timing (10x for small ones)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline estimate")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="seconds of oracle time for the whole --impl reference run")
