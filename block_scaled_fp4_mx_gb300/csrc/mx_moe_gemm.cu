@@ -58,6 +58,7 @@
 #include "fp4_decode.cuh"
 #include "fp4mx.h"
 #include "launch.h"
+#include "moe_act.cuh"
 #include "tc_sm103.cuh"
 
 namespace fp4mx {
@@ -73,8 +74,24 @@ constexpr int kXExtBox = 64;                // activation rows per box of a slab
 constexpr int kXExtBytes = kXExtBox * kK * 2;  // 8 KiB
 
 template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_, bool kGateUp_ = false,
-          int kExt_ = 0, int kDecodeWarps_ = 16, int kEpiWarps_ = 4>
+          int kExt_ = 0, int kDecodeWarps_ = 16, int kEpiWarps_ = 4, bool kMmaSleep_ = false,
+          int kIssuers_ = 1>
 struct TmemCfg {
+    // MMA issuing threads. One thread issues tcgen05.mma at a fixed rate per
+    // instruction whatever N is (measured on GB300: ~145 cycles per 128 x 16 x 16
+    // MMA, ~190 with 16 busy warps beside it, and the rate scales with the number
+    // of issuing threads in different warps), so with few tokens per expert one
+    // issuer cannot keep up with the decoders. With kIssuers = 4 the four epilogue
+    // warps (one per SM sub-partition) issue too: issuer i takes the K slices of
+    // decoder group i into a partial accumulator of its own, and at the end of an item
+    // each of the four warps sums the four partials (in a fixed order) for its TMEM
+    // lane quarter. (Issuers in warps of their own, with the epilogue apart and two
+    // sets of partials, measured slower: 26 warps leave 72 registers a thread.)
+    static constexpr int kIssuers = kIssuers_;
+    // the MMA thread waits for full stages asleep (suspend-time hint) instead of
+    // polling: where a slice holds little MMA work, a polling MMA thread takes the
+    // issue slots of the decoder warps that share its SM sub-partition
+    static constexpr bool kMmaSleep = kMmaSleep_;
     // warp roles: decoders, epilogue (a multiple of 4: kEpiWarps / 4 warps share
     // each TMEM lane quarter and take its chunks in turn), the activation TMA
     // thread, the weight TMA thread and the MMA thread
@@ -83,8 +100,8 @@ struct TmemCfg {
     static constexpr int kEpiWarps = kEpiWarps_;
     static constexpr int kTmaXWarp = kEpiWarp0 + kEpiWarps;
     static constexpr int kTmaWWarp = kTmaXWarp + 1;
-    static constexpr int kMmaWarp = kTmaWWarp + 1;
-    static constexpr int kThreads = (kMmaWarp + 1) * 32;
+    static constexpr int kMmaWarp = kIssuers == 1 ? kTmaWWarp + 1 : -1;
+    static constexpr int kThreads = (kIssuers == 1 ? kMmaWarp + 1 : kTmaWWarp + 1) * 32;
     static constexpr int kTok = kTok_;        // tokens per item (MMA N)
     // an expert's last slab may take up to kExt more tokens (a second MMA per K step
     // into accumulator columns kTok.., same decoded weights), so that rows just past
@@ -108,9 +125,10 @@ struct TmemCfg {
     static constexpr int kBoxRows = kHalves ? kWM / 2 : kGateUp ? kWM : kWRows;  // rows per weight TMA box
     static constexpr int kWarpsPerSlice = 4 * kMTw;
     static constexpr int kGroups = kDecodeWarps / kWarpsPerSlice;
-    // tensor memory: accumulator buffers, then the ring of decoded slices
+    // tensor memory: accumulator buffers (kIssuers partials each), then the ring of
+    // decoded slices
     static constexpr int kAccCols = kMTw * (kTok + kExt);
-    static constexpr int kAColBase = kAccBufs * kAccCols;
+    static constexpr int kAColBase = kAccBufs * kIssuers * kAccCols;
     static constexpr int kAStageCols = kMTw * (kK / 2);
     // shared memory from a 1024-byte aligned base
     static constexpr int kXBytes = (kTok + kExt) * kK * 2;
@@ -122,8 +140,13 @@ struct TmemCfg {
     // per-expert prefix of live token slabs (the compact item list), after the
     // barriers, the TMEM address word and the abort flag
     static constexpr int kOffPrefix = kOffBar + 8 * kNumBars + 16;
-    static constexpr int kSmemBytes = 1024 + kOffPrefix + 4 * (kPrefixExperts + 1);
-    static_assert(kTok == 128 || kTok == 256, "MMA N");
+    // the scaled byte tables of all 256 E8M0 values (16 bytes each), built once per
+    // CTA, where shared memory has room: a decoder thread then loads its two blocks'
+    // tables instead of building them
+    static constexpr int kOffTab = (kOffPrefix + 4 * (kPrefixExperts + 1) + 15) & ~15;
+    static constexpr bool kSmemTable = 1024 + kOffTab + 4096 <= 232448;
+    static constexpr int kSmemBytes = 1024 + (kSmemTable ? kOffTab + 4096 : kOffTab);
+    static_assert(kTok == 64 || kTok == 128 || kTok == 256, "MMA N");
     static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
     static_assert(kExt == 0 || (kExt == kXExtBox && kMTw == 1 && kTok == 256), "slab extension");
     static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
@@ -131,10 +154,28 @@ struct TmemCfg {
     // a decoder group's ring positions advance by kGroups per slice and wrap with
     // one subtraction, so neither ring may be shorter than kGroups
     static_assert(kGroups <= S && kGroups <= SR, "ring depth below the decoder group count");
-    static_assert(kAColBase + S * kAStageCols <= (int)kTmemCols, "tensor memory columns");
+    // one issuer: accumulators and the whole ring fit; several: 16-column partials and
+    // the whole ring fit, and 64-column partials leave at least 8 ring stages
+    static_assert(kIssuers == 1 ? kAColBase + S * kAStageCols <= (int)kTmemCols
+                                : kIssuers * 16 + S * kAStageCols <= (int)kTmemCols &&
+                                      kIssuers * 64 + 8 * kAStageCols <= (int)kTmemCols,
+                  "tensor memory columns");
     static_assert(kSmemBytes <= 232448, "shared memory per block");
+    // several issuers: four (one per decoder group and epilogue warp), one weight tile,
+    // one accumulator buffer, ring stages in whole rounds of the four groups
+    static_assert(kIssuers == 1 || (kIssuers == 4 && kGroups == 4 && kEpiWarps == 4 && kMTw == 1 &&
+                                    kAccBufs == 1 && kExt == 0 && S % 4 == 0 && kEpiWarp0 % 4 == 0),
+                  "issuer layout");
 };
 
+// Up to 32 tokens per expert (decode-time batches): one 128-row weight tile per
+// item (more items than SMs several times over), the MMA's N cut to the expert's
+// tokens rounded up to 16, activation boxes only as tall as the capacity, four MMA
+// issuers with partial accumulators of the capacity rounded up to 16 columns each,
+// and a ring of decoded slices of 12 stages (three per decoder group). (From 33 to 64
+// tokens this configuration measured faster than the next one on the down GEMM and
+// slower on the gate/up GEMM; the next one takes them.)
+using CfgTiny = TmemCfg<64, 1, 1, 12, 24, false, 0, 16, 4, false, 4>;
 // Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
 using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
 // More tokens: 256 tokens per item (an expert's last slab up to 320) against one
@@ -143,6 +184,8 @@ using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
 using CfgLarge = TmemCfg<256, 1, 1, 5, 5, false, 64, 12, 8>;
 // Gate/up GEMM of the MoE layer with the activation function in the epilogue.
 using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true>;
+// The same for up to 64 tokens per expert: gate and up halves of one weight tile.
+using CfgGateUpTiny = TmemCfg<64, 1, 1, 12, 24, true, 0, 16, 4, false, 4>;
 // The same with 256-token slabs (the last up to 320): gate and up halves of one
 // weight tile.
 using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 5, true, 64, 12, 8>;
@@ -194,15 +237,6 @@ __device__ __forceinline__ Item item_compact(int64_t t, int n_tiles, int tok, in
     return it;
 }
 
-// silu(g) * u of two fp32 accumulator words: g / (1 + e^-g) * u in fp32 with the
-// fast exponential and division intrinsics (relative error well below 2^-15 of the
-// result, far under the bf16 rounding that follows; a gate below about -87 gives
-// e^-g = inf and a signed zero).
-__device__ __forceinline__ float silu_mul(uint32_t gate_bits, uint32_t up_bits) {
-    const float g = __uint_as_float(gate_bits);
-    return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), __uint_as_float(up_bits));
-}
-
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
 mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
@@ -211,8 +245,10 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                         const int64_t *__restrict__ expert_offsets,
                         const uint8_t *__restrict__ w_scales, int32_t experts, int64_t max_rows,
                         int64_t total_rows, int32_t n_rows, int32_t n_out, int32_t k,
-                        uint16_t *__restrict__ out, int32_t *__restrict__ status) {
-    // n_rows: weight rows per expert (2 n_out in gate/up mode); n_out: output columns
+                        int32_t x_box_rows, uint16_t *__restrict__ out,
+                        int32_t *__restrict__ status) {
+    // n_rows: weight rows per expert (2 n_out in gate/up mode); n_out: output columns;
+    // x_box_rows: rows of map_x's box (kXBox, or fewer with 64-token items)
     constexpr int kTok = C::kTok, kMTw = C::kMTw, S = C::S, SR = C::SR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -287,16 +323,22 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             mbar_init(empty_raw(s), C::kWarpsPerSlice);
         }
         for (int b = 0; b < C::kAccBufs; ++b) {
-            mbar_init(acc_full(b), 1);
+            mbar_init(acc_full(b), C::kIssuers);  // one commit per issuer
             mbar_init(acc_empty(b), C::kEpiWarps);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(drain_bar, C::kIssuers);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
         if (C::kExt > 0)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x_ext)) : "memory");
+    }
+    if (C::kSmemTable) {
+        for (int e = tid; e < 256; e += C::kThreads) {
+            const ByteTable t = mx_scaled_table((uint32_t)e);
+            st_shared_v4(base + C::kOffTab + 16u * (uint32_t)e, make_uint4(t.lo_a, t.lo_b, t.hi_a, t.hi_b));
+        }
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -309,6 +351,18 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // with several issuers each partial accumulator takes the capacity's columns
+    // (x_box_rows) and the ring of decoded slices takes what is left, in whole
+    // rounds of the four decoder groups (at most S stages)
+    const int acc_stride = C::kIssuers > 1 ? x_box_rows : C::kAccCols;
+    const int a_base = C::kIssuers > 1 ? C::kIssuers * acc_stride : C::kAColBase;
+    const int s_ring =
+        C::kIssuers > 1
+            ? ((((int)kTmemCols - a_base) / C::kAStageCols) & ~3) < S
+                  ? ((((int)kTmemCols - a_base) / C::kAStageCols) & ~3)
+                  : S
+            : S;
+    const uint32_t tab = base + C::kOffTab;
     const int64_t n_items = compact ? (int64_t)prefix[experts] * n_tiles
                                     : (int64_t)experts * slabs * n_tiles;
     auto item = [&](int64_t t) {
@@ -326,14 +380,14 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         // its row of the packed slice in shared memory: the halves layout takes gate
         // row i from box row i and up row i from box row 64 + i
         const int raw_r = C::kHalves ? (lane >> 4) * (kWM / 2) + quarter * 16 + (lane & 15) : r;
-        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)C::kAColBase +
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a_base +
                                    (uint32_t)(mt * (kK / 2));
         bool stop = false;
         uint32_t g0 = 0;  // first slice of the current item
         // ring positions of this group's next slice g (the group's slices are g =
         // group, group + kGroups, ... across items): stage and phase of each ring
-        int sr = group % SR, sw = group % S;
-        uint32_t pr = (uint32_t)(group / SR) & 1u, pw = (uint32_t)(group / S) & 1u;
+        int sr = group % SR, sw = group % s_ring;
+        uint32_t pr = (uint32_t)(group / SR) & 1u, pw = (uint32_t)(group / s_ring) & 1u;
         uint32_t g = (uint32_t)group;
         for (int64_t t = blockIdx.x; t < n_items && !stop; t += gridDim.x) {
             const Item it = item(t);
@@ -368,8 +422,15 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 const uint4 w1 = lds_v4(raw_row + 16u);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_raw(sr));  // the slice's codes are in registers
-                const ByteTable t0 = mx_scaled_table(e0);
-                const ByteTable t1 = mx_scaled_table(e1);
+                ByteTable t0, t1;
+                if constexpr (C::kSmemTable) {
+                    const uint4 q0 = lds_v4(tab + 16u * e0), q1 = lds_v4(tab + 16u * e1);
+                    t0 = ByteTable{q0.x, q0.y, q0.z, q0.w};
+                    t1 = ByteTable{q1.x, q1.y, q1.z, q1.w};
+                } else {
+                    t0 = mx_scaled_table(e0);
+                    t1 = mx_scaled_table(e1);
+                }
                 uint32_t d[32];
                 const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
@@ -380,7 +441,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     d[4 * q + 2] = v.z;
                     d[4 * q + 3] = v.w;
                 }
-                if (g >= (uint32_t)S && lane == 0 && !mbar_wait_sleep(empty(sw), pw ^ 1u))
+                if (g >= (uint32_t)s_ring && lane == 0 && !mbar_wait_sleep(empty(sw), pw ^ 1u))
                     *abort_flag = 1;
                 if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) {
                     stop = true;
@@ -394,7 +455,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 if (lane == 0) mbar_arrive(full(sw));
                 g += C::kGroups;
                 if ((sr += C::kGroups) >= SR) { sr -= SR; pr ^= 1u; }
-                if ((sw += C::kGroups) >= S) { sw -= S; pw ^= 1u; }
+                if ((sw += C::kGroups) >= s_ring) { sw -= s_ring; pw ^= 1u; }
             }
             g0 += (uint32_t)nk;
         }
@@ -406,25 +467,42 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         constexpr int kEpiSubs = C::kEpiWarps / 4;
         const int quarter = warp & 3;
         const int sub = (warp - C::kEpiWarp0) >> 2;
-        uint32_t use[2] = {0, 0};
-        uint32_t j = 0;  // live items so far
-        for (int64_t t = blockIdx.x; t < n_items; t += gridDim.x) {
-            const Item it = item(t);
-            if (!it.live) continue;
-            const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
-            const uint32_t u = b ? use[1] : use[0];
-            if (lane == 0 && !mbar_wait_sleep(acc_full(b), u & 1u)) *abort_flag = 1;
-            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
-            tc_fence_after();
-            auto release = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty(b));
-            };
+        // 32 accumulator columns of this thread's lane at `col`: with several issuers
+        // the sum of the partials in `pmask`, in issuer order (fp32, round to nearest)
+        auto ld32 = [&](uint32_t col, uint32_t(&v)[32], uint32_t pmask) {
+            if constexpr (C::kIssuers == 1) {
+                tmem_ld32(col, v);
+            } else {
+                bool first = true;
+#pragma unroll 1
+                for (int p = 0; p < C::kIssuers; ++p) {
+                    if (!((pmask >> p) & 1u)) continue;
+                    const uint32_t pc = col + (uint32_t)(p * acc_stride);
+                    if (first) {
+                        tmem_ld32(pc, v);
+                        first = false;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t w[16];
+                            tmem_ld16(pc + (uint32_t)(16 * h), w);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[16 * h + i] = __float_as_uint(
+                                    __fadd_rn(__uint_as_float(v[16 * h + i]), __uint_as_float(w[i])));
+                        }
+                    }
+                }
+            }
+        };
+        // read-out of one item from accumulator buffer b; `release` is called after
+        // this warp's last tcgen05.ld of the item
+        auto read_out = [&](const Item &it, int b, uint32_t pmask, auto &&release) {
             const int n_tok = item_tokens(it);  // > 0
             const bool odd = lane & 1;
             const int64_t step2 = 2 * (int64_t)n_out;
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * C::kAccCols);
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
+                                   (uint32_t)(b * C::kIssuers * C::kAccCols);
             uint16_t *const obase = out + (it.row_begin + it.m0 + (odd ? 1 : 0)) * n_out;
             if constexpr (C::kHalves) {
                 // lanes 0-15 of a warp hold gate rows and lanes 16-31 the up rows of
@@ -441,7 +519,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 for (int q = sub; q < chunks; q += kEpiSubs) {
                     const int c0 = q * 32;
                     uint32_t v[32];
-                    tmem_ld32(taddr + (uint32_t)c0, v);
+                    ld32(taddr + (uint32_t)c0, v, pmask);
                     if (q + kEpiSubs >= chunks) release();
                     uint16_t *optr = obase + (int64_t)(c0 + t_half) * n_out + col;
                     const int lim = n_tok - c0 - t_half - (odd ? 1 : 0);
@@ -499,7 +577,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     const int mt = kMTw == 1 ? 0 : q / per_tile;
                     const int c0 = (q - mt * per_tile) * 32;
                     uint32_t acc[32];
-                    tmem_ld32(taddr + (uint32_t)(mt * kTok + c0), acc);
+                    ld32(taddr + (uint32_t)(mt * kTok + c0), acc, pmask);
                     if (q + kEpiSubs >= chunks) release();
                     const int col = it.n0 + mt * kWM + quarter * 32 + (lane & ~1);
                     const bool col_ok = col < n_out;
@@ -516,8 +594,87 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     }
                 }
             }
-            if (b) ++use[1]; else ++use[0];
-            ++j;
+        };
+        if constexpr (C::kIssuers == 1) {
+            uint32_t use[2] = {0, 0};
+            uint32_t j = 0;  // live items so far
+            for (int64_t t = blockIdx.x; t < n_items; t += gridDim.x) {
+                const Item it = item(t);
+                if (!it.live) continue;
+                const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
+                const uint32_t u = b ? use[1] : use[0];
+                if (lane == 0 && !mbar_wait_sleep(acc_full(b), u & 1u)) *abort_flag = 1;
+                if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+                tc_fence_after();
+                read_out(it, b, 1u, [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty(b));
+                });
+                if (b) ++use[1]; else ++use[0];
+                ++j;
+            }
+        } else {
+            // ---- issuer i = this warp's lane quarter: the item's K slices of decoder
+            // group i (slices g = i mod 4 of this CTA's count) into partial accumulator
+            // i, then the read-out of lane quarter i over all partials ----
+            const int me = quarter;
+            const uint32_t d_col = tmem + (uint32_t)(me * acc_stride);
+            const uint32_t a_col0 = tmem + (uint32_t)a_base;
+            const uint64_t x_desc0 = kmajor_sw128_desc(x_ring);
+            uint32_t g0 = 0;          // this CTA's slices before the current item
+            uint32_t items_done = 0;  // live items read out so far
+            for (int64_t t = blockIdx.x; t < n_items; t += gridDim.x) {
+                const Item it = item(t);
+                if (it.bad && me == 0 && lane == 0) atomicExch(status, FP4_ERR_SHAPE);
+                if (!it.live) continue;
+                const int n_tok = item_tokens(it);
+                const uint32_t idesc =
+                    instr_desc_bf16<kWM, 16>() + ((uint32_t)(((n_tok + 15) & ~15) - 16) >> 3 << 17);
+                const int kt0 = (int)(((uint32_t)me + 4u - (g0 & 3u)) & 3u);  // first slice of mine
+                // the previous item's partials must have been read out by all four warps
+                if (items_done > 0 && lane == 0 &&
+                    !mbar_wait_sleep(acc_empty(0), (items_done - 1u) & 1u))
+                    *abort_flag = 1;
+                if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    for (int kt = kt0; kt < nk; kt += 4) {
+                        const uint32_t gg = g0 + (uint32_t)kt;
+                        const int st = (int)(gg % (uint32_t)s_ring);
+                        if (!mbar_wait_bounded(full(st), (gg / (uint32_t)s_ring) & 1u)) {
+                            *abort_flag = 1;
+                            break;
+                        }
+                        tc_fence_after();
+                        mma_slice_tmem_a_commit(d_col, a_col0 + (uint32_t)(st * C::kAStageCols),
+                                                x_desc0 + (uint64_t)(st * (C::kXBytes >> 4)), idesc,
+                                                kt > kt0 ? 1u : 0u, empty(st));
+                    }
+                    mma_commit(acc_full(0));  // arrives once this issuer's MMAs are complete
+                }
+                __syncwarp();
+                if (*abort_flag) break;
+                // the partials of the issuers that had a slice of this item
+                uint32_t pmask = 0;
+                for (int p = 0; p < C::kIssuers; ++p)
+                    if ((int)(((uint32_t)p + 4u - (g0 & 3u)) & 3u) < nk) pmask |= 1u << p;
+                g0 += (uint32_t)nk;
+                if (lane == 0 && !mbar_wait_sleep(acc_full(0), items_done & 1u)) *abort_flag = 1;
+                if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+                tc_fence_after();
+                read_out(it, 0, pmask, [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty(0));
+                });
+                ++items_done;
+            }
+            // every MMA this thread issued completes before tensor memory is released
+            if (lane == 0) {
+                mma_commit(drain_bar);
+                if (!mbar_wait_bounded(drain_bar, 0)) *abort_flag = 1;
+            }
         }
     } else if (warp == C::kTmaXWarp && lane == 0) {
         // ---- TMA: activation tiles ----
@@ -533,7 +690,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             // path, and a branch for the extension box in the plain loop costs ~10%
             if (C::kExt > 0 && n_tok > kTok) {
                 for (int kt = 0; kt < nk; ++kt, ++g) {
-                    if (g >= (uint32_t)S && !mbar_wait_sleep(empty(s), ph ^ 1u)) *abort_flag = 1;
+                    if (g >= (uint32_t)s_ring && !mbar_wait_sleep(empty(s), ph ^ 1u)) *abort_flag = 1;
                     if (*abort_flag) {
                         stop = true;
                         break;
@@ -544,22 +701,24 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                                     row0 + bx * kXBox, full(s));
                     tma_load_2d(x_ring + s * C::kXBytes + kTok / kXBox * kXBoxBytes, &map_x_ext,
                                 kt * kK, row0 + kTok, full(s));
-                    if (++s == S) { s = 0; ph ^= 1u; }
+                    if (++s == s_ring) { s = 0; ph ^= 1u; }
                 }
                 continue;
             }
-            const int boxes = tok_live(n_tok) / kXBox;
+            // 64-token items: one box of x_box_rows rows; else tok_live / 128 boxes
+            const int boxes = kTok == 64 ? 1 : tok_live(n_tok) / kXBox;
+            const uint32_t box_bytes = kTok == 64 ? (uint32_t)x_box_rows * (kK * 2) : (uint32_t)kXBoxBytes;
             for (int kt = 0; kt < nk; ++kt, ++g) {
-                if (g >= (uint32_t)S && !mbar_wait_sleep(empty(s), ph ^ 1u)) *abort_flag = 1;
+                if (g >= (uint32_t)s_ring && !mbar_wait_sleep(empty(s), ph ^ 1u)) *abort_flag = 1;
                 if (*abort_flag) {
                     stop = true;
                     break;
                 }
-                mbar_arrive_expect_tx(full(s), (uint32_t)(boxes * kXBoxBytes));
+                mbar_arrive_expect_tx(full(s), (uint32_t)boxes * box_bytes);
                 for (int bx = 0; bx < boxes; ++bx)
                     tma_load_2d(x_ring + s * C::kXBytes + bx * kXBoxBytes, &map_x, kt * kK,
                                 row0 + bx * kXBox, full(s));
-                if (++s == S) { s = 0; ph ^= 1u; }
+                if (++s == s_ring) { s = 0; ph ^= 1u; }
             }
         }
     } else if (warp == C::kTmaWWarp && lane == 0) {
@@ -585,7 +744,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 if (++s == SR) { s = 0; ph ^= 1u; }
             }
         }
-    } else if (warp == C::kMmaWarp && lane == 0) {
+    } else if (C::kIssuers == 1 && warp == C::kMmaWarp && lane == 0) {
         // ---- MMA issue ----
         constexpr uint32_t idesc_full = instr_desc_bf16<kWM, kTok>();
         constexpr uint32_t idesc_half = instr_desc_bf16<kWM, 128>();
@@ -603,20 +762,26 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             if (it.bad) atomicExch(status, FP4_ERR_SHAPE);
             if (!it.live) continue;
             const int n_tok = item_tokens(it);
-            const uint32_t idesc = tok_live(n_tok) == kTok ? idesc_full : idesc_half;
+            // 64-token items: N = the item's tokens rounded up to 16
+            const uint32_t idesc =
+                kTok == 64 ? instr_desc_bf16<kWM, 16>() + ((uint32_t)(((n_tok + 15) & ~15) - 16) >> 3 << 17)
+                           : (tok_live(n_tok) == kTok ? idesc_full : idesc_half);
             // an extended slab: tokens kTok.. (N rounded up to 16) into columns kTok..
             const int n_ext = C::kExt > 0 && n_tok > kTok ? (n_tok - kTok + 15) & ~15 : 0;
             const uint32_t idesc_ext = instr_desc_bf16<kWM, 16>() + ((uint32_t)(n_ext - 16) >> 3 << 17);
             const int b = C::kAccBufs == 1 ? 0 : (int)(j & 1u);
             const uint32_t u = b ? use[1] : use[0];
             // the buffer's previous item must have been read out
-            if (u > 0 && !mbar_wait_bounded(acc_empty(b), (u - 1u) & 1u)) *abort_flag = 1;
+            if (u > 0 && !(C::kMmaSleep ? mbar_wait_sleep(acc_empty(b), (u - 1u) & 1u)
+                                        : mbar_wait_bounded(acc_empty(b), (u - 1u) & 1u)))
+                *abort_flag = 1;
             const uint32_t d_col = tmem + (uint32_t)(b * C::kAccCols);
             // separate K loops for extended and plain slabs: every instruction of this
             // thread is tensor-pipe idle time, so the common loop carries no extra branch
             if (C::kExt > 0 && n_ext > 0) {
                 for (int kt = 0; kt < nk; ++kt) {
-                    if (!ready && !mbar_wait_bounded(full(st), ph)) {
+                    if (!ready && !(C::kMmaSleep ? mbar_wait_sleep(full(st), ph)
+                                                 : mbar_wait_bounded(full(st), ph))) {
                         *abort_flag = 1;
                         break;
                     }
@@ -633,7 +798,8 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 }
             } else {
                 for (int kt = 0; kt < nk; ++kt) {
-                    if (!ready && !mbar_wait_bounded(full(st), ph)) {
+                    if (!ready && !(C::kMmaSleep ? mbar_wait_sleep(full(st), ph)
+                                                 : mbar_wait_bounded(full(st), ph))) {
                         *abort_flag = 1;
                         break;
                     }
@@ -689,15 +855,16 @@ int sm_count() {
 // columns past k read as zero) and of the packed
 // weights [experts * n_rows, k / 2] uint8 (32-byte x box_rows boxes, no swizzle).
 cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_t *w_packed,
-                             int64_t experts, int64_t n_rows, int64_t k, int box_rows, CUtensorMap *map_x,
-                             CUtensorMap *map_x_ext, CUtensorMap *map_w) {
+                             int64_t experts, int64_t n_rows, int64_t k, int box_rows,
+                             int x_box_rows, CUtensorMap *map_x, CUtensorMap *map_x_ext,
+                             CUtensorMap *map_w) {
     EncodeTiled encode = tensor_map_encoder();
     if (encode == nullptr) return cudaErrorNotSupported;
     const cuuint32_t elem_strides[2] = {1, 1};
     {
         const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)(total_rows > 0 ? total_rows : 1)};
         const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-        const cuuint32_t box[2] = {kK, kXBox};
+        const cuuint32_t box[2] = {kK, (cuuint32_t)x_box_rows};
         if (encode(map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a), dims,
                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -738,9 +905,12 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
         if (err != cudaSuccess) return err;
         configured_device = device;
     }
+    // 64-token items load activation boxes of the capacity rounded up to 16 rows
+    const int x_box_rows =
+        C::kTok == 64 ? (int)(((max_rows < 1 ? 1 : max_rows) + 15) & ~(int64_t)15) : kXBox;
     CUtensorMap map_x, map_x_ext, map_w;
     err = tmem_tensor_maps(a, total_rows, w_packed, experts, n_rows, k,
-                           C::kBoxRows, &map_x, &map_x_ext, &map_w);
+                           C::kBoxRows, x_box_rows, &map_x, &map_x_ext, &map_w);
     if (err != cudaSuccess) return err;
     const int64_t items = experts * ((max_rows + C::kTok - 1) / C::kTok) *
                           ((n_out + C::kTileCols - 1) / C::kTileCols);
@@ -750,7 +920,7 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
     const int grid = (int)(items < sms ? items : sms);
     mx_moe_gemm_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
         map_x, map_x_ext, map_w, expert_offsets, w_scales, (int32_t)experts, max_rows, total_rows,
-        (int32_t)n_rows, (int32_t)n_out, (int32_t)k, out, status);
+        (int32_t)n_rows, (int32_t)n_out, (int32_t)k, (int32_t)x_box_rows, out, status);
     return cudaGetLastError();
 }
 
@@ -763,6 +933,9 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
     if (max_rows > 128)
         return launch_tmem<CfgLarge>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
                                      w_scales, n, n, k, out, status, stream);
+    if (max_rows <= 32)
+        return launch_tmem<CfgTiny>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
+                                    w_scales, n, n, k, out, status, stream);
     return launch_tmem<CfgSmall>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
                                  w_scales, n, n, k, out, status, stream);
 }
@@ -774,6 +947,9 @@ cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offse
     if (max_rows > 128)
         return launch_tmem<CfgGateUpLarge>(x, expert_offsets, experts, max_rows, total_rows,
                                            w1_packed, w1_scales, 2 * n, n, k, act, status, stream);
+    if (max_rows <= 32)
+        return launch_tmem<CfgGateUpTiny>(x, expert_offsets, experts, max_rows, total_rows,
+                                          w1_packed, w1_scales, 2 * n, n, k, act, status, stream);
     return launch_tmem<CfgGateUp>(x, expert_offsets, experts, max_rows, total_rows, w1_packed,
                                   w1_scales, 2 * n, n, k, act, status, stream);
 }

@@ -236,6 +236,13 @@ def test_full_size_layer_sampled_tokens(oracle_impl):
     assert not bad.any(), (int(bad.sum()), float(err.max()))
 
 
+def test_decode_step_layer(oracle_impl):
+    """A decode-time step: 8 tokens, top-4 of 8 experts, hidden = intermediate = 2880
+    (four tokens or so per expert: both GEMMs take one 128-row weight tile per item,
+    N = 16 MMAs from four issuers into partial accumulators)."""
+    check(oracle_impl, make_layer(8, 2880, 2880, 8, 4, seed=35))
+
+
 def test_gpt_oss_like_layer(oracle_impl):
     """Hidden 2880, intermediate 2880, 4 experts, top-4 of 64 tokens."""
     check(oracle_impl, make_layer(64, 2880, 2880, 4, 4, seed=31))

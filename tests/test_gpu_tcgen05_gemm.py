@@ -95,6 +95,26 @@ def test_identity_weights_exact(oracle_impl):
     assert np.array_equal(got, oracle_pins._bf16_bits(exact))
 
 
+@pytest.mark.parametrize("rows,n,k", [([8] * 4, 704, 2880), ([1, 2, 15, 16, 17], 224, 320),
+                                      ([32, 0, 31, 33], 384, 704), ([64, 63, 48, 49], 160, 1088),
+                                      ([40, 3], 128, 64)])
+def test_decode_sized_batches(oracle_impl, rows, n, k):
+    """Decode-time batches. Up to 32 tokens per expert: one 128-row weight tile per
+    item, MMA N = the expert's tokens rounded up to 16, activation boxes of the
+    capacity rounded up to 16 rows, four MMA issuers each summing a quarter of the K
+    slices into a partial accumulator, read out as the sum of the partials; 33 to 64
+    tokens: the 128-token configuration. Ragged n (last tiles of 64, 96 and 32 rows)
+    and an empty expert included."""
+    run_case(oracle_impl, rows, n, k, seed=sum(rows) + n + k)
+
+
+@pytest.mark.parametrize("tokens", [8, 32])
+def test_decode_sized_full_moe_shape(oracle_impl, tokens):
+    """32 experts x 8 or 32 tokens against the gate+up weights [32, 5760, 2880] (the
+    benchmark's decode-sized workloads): the whole output against the oracle."""
+    run_case(oracle_impl, [tokens] * 32, 5760, 2880, seed=17 + tokens)
+
+
 def test_moe_gate_up_shape(oracle_impl):
     """32 experts x 128 tokens against the gate+up weights [32, 5760, 2880]."""
     run_case(oracle_impl, [128] * 32, 5760, 2880, seed=7)
