@@ -100,8 +100,11 @@ struct TmemCfg {
     static constexpr int kEpiWarps = kEpiWarps_;
     static constexpr int kTmaXWarp = kEpiWarp0 + kEpiWarps;
     static constexpr int kTmaWWarp = kTmaXWarp + 1;
+    // with one accumulator per item, one MMA warp per 128-row weight tile: each issues
+    // its tile's MMAs into its own accumulator columns, so two tiles take two issuers
+    static constexpr int kTileIssuers = kIssuers == 1 ? kMTw_ : 1;
     static constexpr int kMmaWarp = kIssuers == 1 ? kTmaWWarp + 1 : -1;
-    static constexpr int kThreads = (kIssuers == 1 ? kMmaWarp + 1 : kTmaWWarp + 1) * 32;
+    static constexpr int kThreads = (kIssuers == 1 ? kMmaWarp + kTileIssuers : kTmaWWarp + 1) * 32;
     static constexpr int kTok = kTok_;        // tokens per item (MMA N)
     // an expert's last slab may take up to kExt more tokens (a second MMA per K step
     // into accumulator columns kTok.., same decoded weights), so that rows just past
@@ -175,17 +178,17 @@ struct TmemCfg {
 // and a ring of decoded slices of 12 stages (three per decoder group). (From 33 to 64
 // tokens this configuration measured faster than the next one on the down GEMM and
 // slower on the gate/up GEMM; the next one takes them.)
-using CfgTiny = TmemCfg<64, 1, 1, 12, 24, false, 0, 16, 4, false, 4>;
+using CfgTiny = TmemCfg<64, 1, 1, 12, 24, false, 0, 16, 4, true, 4>;
 // Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
-using CfgSmall = TmemCfg<128, 2, 1, 4, 8>;
+using CfgSmall = TmemCfg<128, 2, 1, 4, 8, false, 0, 16, 4, true>;
 // More tokens: 256 tokens per item (an expert's last slab up to 320) against one
 // weight tile; 12 decoder warps (3 groups) and 8 epilogue warps, so that the
 // single accumulator is read out twice as fast at the end of an item.
 using CfgLarge = TmemCfg<256, 1, 1, 5, 5, false, 64, 12, 8>;
 // Gate/up GEMM of the MoE layer with the activation function in the epilogue.
-using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true>;
+using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true, 0, 16, 4, true>;
 // The same for up to 64 tokens per expert: gate and up halves of one weight tile.
-using CfgGateUpTiny = TmemCfg<64, 1, 1, 12, 24, true, 0, 16, 4, false, 4>;
+using CfgGateUpTiny = TmemCfg<64, 1, 1, 12, 24, true, 0, 16, 4, true, 4>;
 // The same with 256-token slabs (the last up to 320): gate and up halves of one
 // weight tile.
 using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 5, true, 64, 12, 8>;
@@ -316,17 +319,17 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         for (int s = 0; s < S; ++s) {
             // the activation TMA thread's arrival (with its bytes) and one per decoder warp
             mbar_init(full(s), C::kWarpsPerSlice + 1);
-            mbar_init(empty(s), 1);
+            mbar_init(empty(s), C::kTileIssuers);  // one commit per MMA warp
         }
         for (int s = 0; s < SR; ++s) {
             mbar_init(full_raw(s), 1);
             mbar_init(empty_raw(s), C::kWarpsPerSlice);
         }
         for (int b = 0; b < C::kAccBufs; ++b) {
-            mbar_init(acc_full(b), C::kIssuers);  // one commit per issuer
+            mbar_init(acc_full(b), C::kIssuers * C::kTileIssuers);  // one commit per issuer
             mbar_init(acc_empty(b), C::kEpiWarps);
         }
-        mbar_init(drain_bar, C::kIssuers);
+        mbar_init(drain_bar, C::kIssuers * C::kTileIssuers);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
@@ -642,7 +645,8 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     for (int kt = kt0; kt < nk; kt += 4) {
                         const uint32_t gg = g0 + (uint32_t)kt;
                         const int st = (int)(gg % (uint32_t)s_ring);
-                        if (!mbar_wait_bounded(full(st), (gg / (uint32_t)s_ring) & 1u)) {
+                        if (!(C::kMmaSleep ? mbar_wait_sleep(full(st), (gg / (uint32_t)s_ring) & 1u)
+                                           : mbar_wait_bounded(full(st), (gg / (uint32_t)s_ring) & 1u))) {
                             *abort_flag = 1;
                             break;
                         }
@@ -744,8 +748,12 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 if (++s == SR) { s = 0; ph ^= 1u; }
             }
         }
-    } else if (C::kIssuers == 1 && warp == C::kMmaWarp && lane == 0) {
-        // ---- MMA issue ----
+    } else if (C::kIssuers == 1 && warp >= C::kMmaWarp && warp < C::kMmaWarp + C::kTileIssuers &&
+               lane == 0) {
+        // ---- MMA issue: weight tile mt of every item (a thread issues one tcgen05.mma
+        // per ~120-200 cycles whatever its N, measured on GB300, so the two 128 x 128
+        // tiles of a 128-token item take one issuer each) ----
+        const int mt = warp - C::kMmaWarp;
         constexpr uint32_t idesc_full = instr_desc_bf16<kWM, kTok>();
         constexpr uint32_t idesc_half = instr_desc_bf16<kWM, 128>();
         // stage 0 descriptors; stage s and K step kk add s * bytes/16 and kk * 32/16
@@ -806,8 +814,9 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     tc_fence_after();
                     const int st_next = st + 1 == S ? 0 : st + 1;
                     const uint32_t ph_next = st + 1 == S ? ph ^ 1u : ph;
-                    ready = mma_slice_tmem_a<kMTw, kTok>(
-                        d_col, a_col0 + (uint32_t)(st * C::kAStageCols),
+                    ready = mma_slice_tmem_a(
+                        d_col + (uint32_t)(mt * kTok),
+                        a_col0 + (uint32_t)(st * C::kAStageCols + mt * (kK / 2)),
                         x_desc0 + (uint64_t)(st * (C::kXBytes >> 4)), idesc, kt > 0 ? 1u : 0u,
                         empty(st), full(st_next), ph_next);
                     st = st_next;

@@ -91,59 +91,30 @@ __device__ __forceinline__ void tc_fence_after() {
 // One K slice of MMAs with A in tensor memory, then a commit to `empty_bar`, with
 // a non-blocking probe of the next stage's barrier (`next_bar`, phase
 // `next_phase`) issued ahead of them so that its latency hides behind the MMA
-// issue. kTiles accumulators (A tiles 32 columns apart, D tiles kN columns
-// apart) each take four K = 16 steps: A advances 8 columns and the B descriptor
-// 32 bytes (2 in its address field) per step. `accumulate` = 0 overwrites D with
-// the first step. Returns whether the probed phase had already completed.
-template <int kTiles, int kN>
+// issue. Four K = 16 steps: A advances 8 columns and the B descriptor 32 bytes
+// (2 in its address field) per step. `accumulate` = 0 overwrites D with the
+// first step. Returns whether the probed phase had already completed.
 __device__ __forceinline__ uint32_t mma_slice_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                      uint32_t idesc, uint32_t accumulate,
                                                      uint32_t empty_bar, uint32_t next_bar,
                                                      uint32_t next_phase) {
-    static_assert(kTiles == 1 || kTiles == 2, "accumulators per slice");
     uint32_t ready;
-    if constexpr (kTiles == 1) {
-        asm volatile(
-            "{\n\t.reg .pred pr, p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 pr, [%7], %8;\n\t"
-            "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
-            "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
-            "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %4, pt;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %4, pt;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %4, pt;\n\t"
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-            "selp.u32 %0, 1, 0, pr;\n\t}"
-            : "=r"(ready)
-            : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar),
-              "r"(next_bar), "r"(next_phase)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred pr, p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t"
-            ".reg .b32 a1, a2, a3, a4, a5, a6, a7, d1;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 pr, [%7], %8;\n\t"
-            "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
-            "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
-            "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
-            "add.u32 a4, %2, 32;\n\tadd.u32 a5, %2, 40;\n\tadd.u32 a6, %2, 48;\n\t"
-            "add.u32 a7, %2, 56;\n\tadd.u32 d1, %1, %9;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %4, pt;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %4, pt;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %4, pt;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a4], %3, %4, p0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a5], b1, %4, pt;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a6], b2, %4, pt;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [d1], [a7], b3, %4, pt;\n\t"
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-            "selp.u32 %0, 1, 0, pr;\n\t}"
-            : "=r"(ready)
-            : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar),
-              "r"(next_bar), "r"(next_phase), "n"(kN)
-            : "memory");
-    }
+    asm volatile(
+        "{\n\t.reg .pred pr, p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pr, [%7], %8;\n\t"
+        "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+        "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+        "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %4, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+        "selp.u32 %0, 1, 0, pr;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar),
+          "r"(next_bar), "r"(next_phase)
+        : "memory");
     return ready;
 }
 
