@@ -37,10 +37,13 @@
 //     warps and the remaining warps form further groups that own every kGroups-th
 //     slice; each thread loads its row's E8M0 bytes from global memory one slice
 //     ahead and takes the packed codes from shared memory;
-//   - one thread issues tcgen05.mma kind::f16 (M = 128, N = kTok, K = 16, A from
-//     TMEM), one asm block per slice that also probes the next stage's barrier
-//     ahead of the MMAs (tcgen05.mma issue blocks at the tensor rate, so every
-//     other instruction of this thread is tensor-pipe idle time);
+//   - MMA issuers: tcgen05.mma kind::f16 (M = 128, N = kTok, K = 16, A from TMEM),
+//     one asm block per slice that also probes the next stage's barrier ahead of
+//     the MMAs. A thread gets one tcgen05.mma issued per ~120-200 SM cycles,
+//     whatever N is (measured on GB300), and issuers in different warps overlap:
+//     one thread per item with one 256-token tile, one per 128-row tile with two
+//     tiles, and four (each summing a quarter of the K slices into a partial
+//     accumulator) for decode-time batches;
 //   - an epilogue warpgroup reads finished accumulators with tcgen05.ld (a thread
 //     holds one weight row, i.e. one output column, for 32 tokens), rounds to
 //     bf16, pairs neighbouring columns with one lane exchange and stores 4-byte
@@ -51,10 +54,11 @@
 //
 // Every mbarrier wait is bounded: a wait that runs out sets an abort flag that
 // every role polls, and the launch reports FP4_ERR_TIMEOUT in the status word
-// after the MMA thread has drained its tensor-core work and TMEM is freed. The
+// after the MMA issuers have drained their tensor-core work and TMEM is freed. The
 // decoders, the epilogue and the TMA threads wait with a suspend-time hint
 // (they sleep instead of spinning, which leaves the issue slots to the MMA
-// thread and the decoders that work: 5-8% faster); the MMA thread spins.
+// thread and the decoders that work: 5-8% faster); the MMA thread of the
+// 256-token configurations polls, the issuers of the others sleep too.
 #include "fp4_decode.cuh"
 #include "fp4mx.h"
 #include "launch.h"
