@@ -79,8 +79,14 @@ constexpr int kXExtBytes = kXExtBox * kK * 2;  // 8 KiB
 
 template <int kTok_, int kMTw_, int kAccBufs_, int kStages_, int kStagesRaw_, bool kGateUp_ = false,
           int kExt_ = 0, int kDecodeWarps_ = 16, int kEpiWarps_ = 4, bool kMmaSleep_ = false,
-          int kIssuers_ = 1>
+          int kIssuers_ = 1, int kKS_ = kK>
 struct TmemCfg {
+    // K per slice: 64, or 128 = two 64-wide sub-slices per stage (two activation boxes,
+    // 128 codes per decoder thread, eight MMAs per commit) where a slice's handshakes
+    // cost more than its work: with decode-time batches the pipeline spends ~2,000
+    // cycles per slice and decoder group even with no decode or MMA (measured on GB300)
+    static constexpr int kKS = kKS_;
+    static constexpr int kSub = kKS_ / kK;
     // MMA issuing threads. One thread issues tcgen05.mma at a fixed rate per
     // instruction whatever N is (measured on GB300: ~145 cycles per 128 x 16 x 16
     // MMA, ~190 with 16 busy warps beside it, and the rate scales with the number
@@ -136,10 +142,11 @@ struct TmemCfg {
     // decoded slices
     static constexpr int kAccCols = kMTw * (kTok + kExt);
     static constexpr int kAColBase = kAccBufs * kIssuers * kAccCols;
-    static constexpr int kAStageCols = kMTw * (kK / 2);
+    static constexpr int kAStageCols = kMTw * (kKS / 2);
     // shared memory from a 1024-byte aligned base
-    static constexpr int kXBytes = (kTok + kExt) * kK * 2;
-    static constexpr int kRawBytes = kWRows * (kK / 2);
+    static constexpr int kXSubBytes = (kTok + kExt) * kK * 2;  // one 64-wide sub-slice
+    static constexpr int kXBytes = kSub * kXSubBytes;
+    static constexpr int kRawBytes = kWRows * (kKS / 2);
     static constexpr int kOffX = 0;
     static constexpr int kOffRaw = kOffX + S * kXBytes;
     static constexpr int kOffBar = kOffRaw + SR * kRawBytes;
@@ -154,6 +161,7 @@ struct TmemCfg {
     static constexpr bool kSmemTable = 1024 + kOffTab + 4096 <= 232448;
     static constexpr int kSmemBytes = 1024 + (kSmemTable ? kOffTab + 4096 : kOffTab);
     static_assert(kTok == 64 || kTok == 128 || kTok == 256, "MMA N");
+    static_assert(kKS == kK || (kKS == 2 * kK && kIssuers == 4 && kMTw == 1), "K per slice");
     static_assert(kMTw == 1 || kMTw == 2, "weight tiles per item");
     static_assert(kExt == 0 || (kExt == kXExtBox && kMTw == 1 && kTok == 256), "slab extension");
     static_assert(kDecodeWarps % kWarpsPerSlice == 0, "decoder groups");
@@ -165,7 +173,8 @@ struct TmemCfg {
     // the whole ring fit, and 64-column partials leave at least 8 ring stages
     static_assert(kIssuers == 1 ? kAColBase + S * kAStageCols <= (int)kTmemCols
                                 : kIssuers * 16 + S * kAStageCols <= (int)kTmemCols &&
-                                      kIssuers * 64 + 8 * kAStageCols <= (int)kTmemCols,
+                                      kIssuers * 64 + 8 * 32 <= (int)kTmemCols &&
+                                      kIssuers * 32 + 4 * kAStageCols <= (int)kTmemCols,
                   "tensor memory columns");
     static_assert(kSmemBytes <= 232448, "shared memory per block");
     // several issuers: four (one per decoder group and epilogue warp), one weight tile,
@@ -182,7 +191,7 @@ struct TmemCfg {
 // and a ring of decoded slices of 12 stages (three per decoder group). (From 33 to 64
 // tokens this configuration measured faster than the next one on the down GEMM and
 // slower on the gate/up GEMM; the next one takes them.)
-using CfgTiny = TmemCfg<64, 1, 1, 12, 24, false, 0, 16, 4, true, 4>;
+using CfgTiny = TmemCfg<64, 1, 1, 4, 12, false, 0, 16, 4, true, 4, 2 * kK>;
 // Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
 using CfgSmall = TmemCfg<128, 2, 1, 4, 8, false, 0, 16, 4, true>;
 // More tokens: 256 tokens per item (an expert's last slab up to 320) against one
@@ -192,7 +201,7 @@ using CfgLarge = TmemCfg<256, 1, 1, 5, 5, false, 64, 12, 8>;
 // Gate/up GEMM of the MoE layer with the activation function in the epilogue.
 using CfgGateUp = TmemCfg<128, 2, 1, 4, 8, true, 0, 16, 4, true>;
 // The same for up to 64 tokens per expert: gate and up halves of one weight tile.
-using CfgGateUpTiny = TmemCfg<64, 1, 1, 12, 24, true, 0, 16, 4, true, 4>;
+using CfgGateUpTiny = TmemCfg<64, 1, 1, 4, 12, true, 0, 16, 4, true, 4, 2 * kK>;
 // The same with 256-token slabs (the last up to 320): gate and up halves of one
 // weight tile.
 using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 5, true, 64, 12, 8>;
@@ -278,7 +287,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     const int lane = tid & 31;
     const int n_tiles = (n_out + C::kTileCols - 1) / C::kTileCols;
     const int slabs = (int)((max_rows + kTok - 1) / kTok);
-    const int nk = (k + kK - 1) / kK;
+    const int nk = (k + C::kKS - 1) / C::kKS;  // K slices
     const int scale_pitch = k / 32;
     // up to kPrefixExperts experts the CTAs walk live items only; beyond, every
     // expert gets max_rows' slabs and dead items are skipped
@@ -388,7 +397,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         // row i from box row i and up row i from box row 64 + i
         const int raw_r = C::kHalves ? (lane >> 4) * (kWM / 2) + quarter * 16 + (lane & 15) : r;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a_base +
-                                   (uint32_t)(mt * (kK / 2));
+                                   (uint32_t)(mt * (C::kKS / 2));
         bool stop = false;
         uint32_t g0 = 0;  // first slice of the current item
         // ring positions of this group's next slice g (the group's slices are g =
@@ -405,28 +414,39 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const int wr = C::kGateUp ? half * n_out + it.n0 + i_tile : it.n0 + r;
             const bool row_ok = C::kGateUp ? it.n0 + i_tile < n_out : wr < n_out;
             const uint8_t *srow = w_scales + ((int64_t)it.expert * n_rows + wr) * scale_pitch;
-            // the row's two E8M0 bytes of slice kt; those of the group's next slice
-            // are loaded one slice ahead, so their latency hides behind a slice
+            // the row's E8M0 bytes of slice kt (kKS / 32 of them); those of the group's
+            // next slice are loaded one slice ahead, so their latency hides behind a slice
             auto scale_at = [&](int kt, int h) {
-                return (row_ok && 2 * kt + h < scale_pitch) ? ldg_early_u8(srow + 2 * kt + h) : 127u;
+                const int b = (C::kKS / 32) * kt + h;
+                return (row_ok && b < scale_pitch) ? ldg_early_u8(srow + b) : 127u;
             };
             const int kt_first = (int)(((uint32_t)group + (uint32_t)C::kGroups -
                                         g0 % (uint32_t)C::kGroups) % (uint32_t)C::kGroups);
-            uint32_t next_e0 = scale_at(kt_first, 0), next_e1 = scale_at(kt_first, 1);
+            uint32_t next_e[2 * C::kSub];
+#pragma unroll
+            for (int h = 0; h < 2 * C::kSub; ++h) next_e[h] = scale_at(kt_first, h);
             for (int kt = kt_first; kt < nk; kt += C::kGroups) {
-                const uint32_t e0 = next_e0, e1 = next_e1;
+                uint32_t ev[2 * C::kSub];
+#pragma unroll
+                for (int h = 0; h < 2 * C::kSub; ++h) ev[h] = next_e[h];
                 if (kt + C::kGroups < nk) {
-                    next_e0 = scale_at(kt + C::kGroups, 0);
-                    next_e1 = scale_at(kt + C::kGroups, 1);
+#pragma unroll
+                    for (int h = 0; h < 2 * C::kSub; ++h) next_e[h] = scale_at(kt + C::kGroups, h);
                 }
+                const uint32_t e0 = ev[0], e1 = ev[1];
                 if (lane == 0 && !mbar_wait_sleep(full_raw(sr), pr)) *abort_flag = 1;
                 if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) {  // warp-uniform
                     stop = true;
                     break;
                 }
-                const uint32_t raw_row = raw_ring + sr * C::kRawBytes + (uint32_t)raw_r * 32u;
+                const uint32_t raw_row = raw_ring + sr * C::kRawBytes + (uint32_t)raw_r * (uint32_t)(C::kKS / 2);
                 const uint4 w0 = lds_v4(raw_row);
                 const uint4 w1 = lds_v4(raw_row + 16u);
+                uint4 w2 = w0, w3 = w1;  // the second sub-slice's codes
+                if constexpr (C::kSub == 2) {
+                    w2 = lds_v4(raw_row + 32u);
+                    w3 = lds_v4(raw_row + 48u);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_raw(sr));  // the slice's codes are in registers
                 ByteTable t0, t1;
@@ -457,6 +477,29 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 tc_fence_after();
                 tmem_st32(lane_addr + (uint32_t)(sw * C::kAStageCols), d);
                 tmem_wait_st();
+                if constexpr (C::kSub == 2) {
+                    // the second 64-wide sub-slice into the next 32 columns
+                    ByteTable t2, t3;
+                    if constexpr (C::kSmemTable) {
+                        const uint4 q2 = lds_v4(tab + 16u * ev[2]), q3 = lds_v4(tab + 16u * ev[3]);
+                        t2 = ByteTable{q2.x, q2.y, q2.z, q2.w};
+                        t3 = ByteTable{q3.x, q3.y, q3.z, q3.w};
+                    } else {
+                        t2 = mx_scaled_table(ev[2]);
+                        t3 = mx_scaled_table(ev[3]);
+                    }
+                    const uint32_t words2[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 v = mx_decode_word(words2[q], q < 4 ? t2 : t3);
+                        d[4 * q + 0] = v.x;
+                        d[4 * q + 1] = v.y;
+                        d[4 * q + 2] = v.z;
+                        d[4 * q + 3] = v.w;
+                    }
+                    tmem_st32(lane_addr + (uint32_t)(sw * C::kAStageCols + kK / 2), d);
+                    tmem_wait_st();
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full(sw));
@@ -655,9 +698,16 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                             break;
                         }
                         tc_fence_after();
-                        mma_slice_tmem_a_commit(d_col, a_col0 + (uint32_t)(st * C::kAStageCols),
-                                                x_desc0 + (uint64_t)(st * (C::kXBytes >> 4)), idesc,
-                                                kt > kt0 ? 1u : 0u, empty(st));
+                        if constexpr (C::kSub == 2) {
+                            const uint64_t xd = x_desc0 + (uint64_t)(st * (C::kXBytes >> 4));
+                            mma_slice2_tmem_a_commit(d_col, a_col0 + (uint32_t)(st * C::kAStageCols), xd,
+                                                     xd + (uint64_t)(C::kXSubBytes >> 4), idesc,
+                                                     kt > kt0 ? 1u : 0u, empty(st));
+                        } else {
+                            mma_slice_tmem_a_commit(d_col, a_col0 + (uint32_t)(st * C::kAStageCols),
+                                                    x_desc0 + (uint64_t)(st * (C::kXBytes >> 4)), idesc,
+                                                    kt > kt0 ? 1u : 0u, empty(st));
+                        }
                     }
                     mma_commit(acc_full(0));  // arrives once this issuer's MMAs are complete
                 }
@@ -713,7 +763,8 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 }
                 continue;
             }
-            // 64-token items: one box of x_box_rows rows; else tok_live / 128 boxes
+            // 64-token items: one box of x_box_rows rows per 64-wide sub-slice; else
+            // tok_live / 128 boxes
             const int boxes = kTok == 64 ? 1 : tok_live(n_tok) / kXBox;
             const uint32_t box_bytes = kTok == 64 ? (uint32_t)x_box_rows * (kK * 2) : (uint32_t)kXBoxBytes;
             for (int kt = 0; kt < nk; ++kt, ++g) {
@@ -722,10 +773,12 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     stop = true;
                     break;
                 }
-                mbar_arrive_expect_tx(full(s), (uint32_t)boxes * box_bytes);
-                for (int bx = 0; bx < boxes; ++bx)
-                    tma_load_2d(x_ring + s * C::kXBytes + bx * kXBoxBytes, &map_x, kt * kK,
-                                row0 + bx * kXBox, full(s));
+                mbar_arrive_expect_tx(full(s), (uint32_t)(C::kSub * boxes) * box_bytes);
+#pragma unroll
+                for (int sub = 0; sub < C::kSub; ++sub)
+                    for (int bx = 0; bx < boxes; ++bx)
+                        tma_load_2d(x_ring + s * C::kXBytes + sub * C::kXSubBytes + bx * kXBoxBytes, &map_x,
+                                    kt * C::kKS + sub * kK, row0 + bx * kXBox, full(s));
                 if (++s == s_ring) { s = 0; ph ^= 1u; }
             }
         }
@@ -745,10 +798,10 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     break;
                 }
                 mbar_arrive_expect_tx(full_raw(s), (uint32_t)C::kRawBytes);
-                tma_load_2d(raw_ring + s * C::kRawBytes, &map_w, kt * (kK / 2), w_row, full_raw(s));
+                tma_load_2d(raw_ring + s * C::kRawBytes, &map_w, kt * (C::kKS / 2), w_row, full_raw(s));
                 if (C::kGateUp)  // the matching up rows fill the second half of the stage
-                    tma_load_2d(raw_ring + s * C::kRawBytes + C::kBoxRows * (kK / 2), &map_w,
-                                kt * (kK / 2), w_row + n_out, full_raw(s));
+                    tma_load_2d(raw_ring + s * C::kRawBytes + C::kBoxRows * (C::kKS / 2), &map_w,
+                                kt * (C::kKS / 2), w_row + n_out, full_raw(s));
                 if (++s == SR) { s = 0; ph ^= 1u; }
             }
         }
@@ -865,11 +918,11 @@ int sm_count() {
 
 // Tensor maps of the activations [total_rows, k] bf16 (64 x 128 boxes and, for
 // slab extensions, 64 x 64 boxes; 128-byte swizzle; rows past total_rows and
-// columns past k read as zero) and of the packed
-// weights [experts * n_rows, k / 2] uint8 (32-byte x box_rows boxes, no swizzle).
+// columns past k read as zero) and of the packed weights [experts * n_rows, k / 2]
+// uint8 (raw_w-byte x box_rows boxes, no swizzle; columns past k / 2 read as zero).
 cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_t *w_packed,
                              int64_t experts, int64_t n_rows, int64_t k, int box_rows,
-                             int x_box_rows, CUtensorMap *map_x, CUtensorMap *map_x_ext,
+                             int x_box_rows, int raw_w, CUtensorMap *map_x, CUtensorMap *map_x_ext,
                              CUtensorMap *map_w) {
     EncodeTiled encode = tensor_map_encoder();
     if (encode == nullptr) return cudaErrorNotSupported;
@@ -893,7 +946,7 @@ cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_
     {
         const cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)(experts * n_rows)};
         const cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
-        const cuuint32_t box[2] = {kK / 2, (cuuint32_t)box_rows};
+        const cuuint32_t box[2] = {(cuuint32_t)raw_w, (cuuint32_t)box_rows};
         if (encode(map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_packed), dims,
                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -923,7 +976,7 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
         C::kTok == 64 ? (int)(((max_rows < 1 ? 1 : max_rows) + 15) & ~(int64_t)15) : kXBox;
     CUtensorMap map_x, map_x_ext, map_w;
     err = tmem_tensor_maps(a, total_rows, w_packed, experts, n_rows, k,
-                           C::kBoxRows, x_box_rows, &map_x, &map_x_ext, &map_w);
+                           C::kBoxRows, x_box_rows, C::kKS / 2, &map_x, &map_x_ext, &map_w);
     if (err != cudaSuccess) return err;
     const int64_t items = experts * ((max_rows + C::kTok - 1) / C::kTok) *
                           ((n_out + C::kTileCols - 1) / C::kTileCols);

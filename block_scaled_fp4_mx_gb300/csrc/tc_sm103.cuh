@@ -139,6 +139,38 @@ __device__ __forceinline__ void mma_slice_tmem_a_commit(uint32_t d_tmem, uint32_
         : "memory");
 }
 
+// Two 64-wide K sub-slices of MMAs with A in tensor memory (eight K = 16 steps: A
+// advances 8 columns per step across both sub-slices; B takes the four steps of each
+// sub-slice from its own descriptor, b_desc and b2_desc) and one commit to
+// `empty_bar`. `accumulate` = 0 overwrites D with the first step.
+__device__ __forceinline__ void mma_slice2_tmem_a_commit(uint32_t d_tmem, uint32_t a_tmem,
+                                                         uint64_t b_desc, uint64_t b2_desc,
+                                                         uint32_t idesc, uint32_t accumulate,
+                                                         uint32_t empty_bar) {
+    asm volatile(
+        "{\n\t.reg .pred p0, pt;\n\t.reg .b64 b1, b2, b3, c1, c2, c3;\n\t"
+        ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+        "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+        "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+        "add.u64 c1, %3, 2;\n\tadd.u64 c2, %3, 4;\n\tadd.u64 c3, %3, 6;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+        "add.u32 a4, %1, 32;\n\tadd.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\t"
+        "add.u32 a7, %1, 56;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], %3, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], c1, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], c2, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], c3, %4, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+        :
+        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "l"(b2_desc), "r"(idesc), "r"(accumulate),
+          "r"(empty_bar)
+        : "memory");
+}
+
 // The single-tile slice of mma_slice_tmem_a with a second accumulator: each K step
 // also multiplies the same A columns with a second B operand (`b2_desc`, e.g. the
 // activation rows past the first N) into `d2_tmem` with its own instruction
