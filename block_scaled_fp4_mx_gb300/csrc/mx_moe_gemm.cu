@@ -440,12 +440,16 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     break;
                 }
                 const uint32_t raw_row = raw_ring + sr * C::kRawBytes + (uint32_t)raw_r * (uint32_t)(C::kKS / 2);
-                const uint4 w0 = lds_v4(raw_row);
-                const uint4 w1 = lds_v4(raw_row + 16u);
+                // 64-byte rows come with the 64-byte swizzle: 16-byte chunk c of row r sits
+                // at chunk c ^ (r / 2 % 4), so that 8 consecutive rows' reads of one chunk
+                // hit 8 different bank groups
+                const uint32_t sw64 = C::kSub == 2 ? (uint32_t)((raw_r >> 1) & 3) : 0u;
+                const uint4 w0 = lds_v4(raw_row + 16u * (0u ^ sw64));
+                const uint4 w1 = lds_v4(raw_row + 16u * (1u ^ sw64));
                 uint4 w2 = w0, w3 = w1;  // the second sub-slice's codes
                 if constexpr (C::kSub == 2) {
-                    w2 = lds_v4(raw_row + 32u);
-                    w3 = lds_v4(raw_row + 48u);
+                    w2 = lds_v4(raw_row + 16u * (2u ^ sw64));
+                    w3 = lds_v4(raw_row + 16u * (3u ^ sw64));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_raw(sr));  // the slice's codes are in registers
@@ -919,7 +923,8 @@ int sm_count() {
 // Tensor maps of the activations [total_rows, k] bf16 (64 x 128 boxes and, for
 // slab extensions, 64 x 64 boxes; 128-byte swizzle; rows past total_rows and
 // columns past k read as zero) and of the packed weights [experts * n_rows, k / 2]
-// uint8 (raw_w-byte x box_rows boxes, no swizzle; columns past k / 2 read as zero).
+// uint8 (raw_w-byte x box_rows boxes: 32 bytes unswizzled, 64 bytes with the 64-byte
+// swizzle; columns past k / 2 read as zero).
 cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_t *w_packed,
                              int64_t experts, int64_t n_rows, int64_t k, int box_rows,
                              int x_box_rows, int raw_w, CUtensorMap *map_x, CUtensorMap *map_x_ext,
@@ -949,7 +954,8 @@ cudaError_t tmem_tensor_maps(const uint16_t *a, int64_t total_rows, const uint8_
         const cuuint32_t box[2] = {(cuuint32_t)raw_w, (cuuint32_t)box_rows};
         if (encode(map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_packed), dims,
                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   raw_w == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
