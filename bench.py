@@ -671,6 +671,31 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def workload_traffic(kind: str, workload: str, elements_per_launch: float):
+    """DRAM bytes (read + write) per launch of one workload from the committed ncu
+    captures in profiles/dram_traffic_by_workload.json, with the capture's command;
+    (None, None) without a capture, (None, "stale") once a listed source changed."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_by_workload.json")
+    try:
+        with open(path) as fh:
+            recs = json.load(fh)
+    except Exception:  # noqa: BLE001
+        return None, None
+    for rec in recs:
+        if rec["kind"] != kind or rec["workload"] != workload:
+            continue
+        if abs(rec["launch_elements"] - elements_per_launch) > 0.5:
+            return None, None
+        h = hashlib.sha256()
+        for rel in rec["sources"]:
+            with open(os.path.join(ROOT, rel), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest()[:16] != rec["source_sha256_16"]:
+            return None, "stale"
+        return rec["dram_bytes_read"] + rec["dram_bytes_write"], rec["capture"]
+    return None, None
+
+
 def ncu_traffic(kind: str, elements_per_launch: float):
     """DRAM bytes per launch of the MXFP4 kernel from the committed ncu capture,
     scaled to this launch size; None for other kernels or once the kernel source
@@ -809,6 +834,15 @@ def run_ours(args, d: Dist):
     for i, op in enumerate(ops):
         rec = {"workload": op_label(op), "kernel": op.kernel, "in_step": True,
                **per_launch_record(op, op_ms[i] / 1e3 / k, peak, tensor_peak)}
+        # DRAM bytes of this launch from a committed ncu capture of the same kernel
+        # source and workload, over this run's in-step time
+        dram, dram_src = workload_traffic(op.kind, rec["workload"], op.elems)
+        if dram is None and op.kind == "mx_unpack":
+            dram, dram_src = ncu_traffic(op.kind, op.elems)
+        if dram is not None:
+            launch_s = op_ms[i] / 1e3 / k
+            rec.update(dram_bytes_per_launch=dram, dram_gbs=dram / launch_s / 1e9,
+                       dram_frac_of_peak=dram / launch_s / 1e9 / peak, dram_source=dram_src)
         configs.append(rec)
     for op in side:
         configs.append({"workload": op_label(op), "kernel": op.kernel, "in_step": False})
