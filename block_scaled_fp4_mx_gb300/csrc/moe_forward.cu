@@ -95,6 +95,7 @@ moe_route_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t experts
 }
 
 // One warp per slot p = m * topk + j.
+constexpr int kScatterVecs = 12;
 __global__ void __launch_bounds__(kThreads)
 moe_scatter_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t topk, int32_t experts,
                    int64_t max_rows, const int32_t *__restrict__ counts,
@@ -113,21 +114,26 @@ moe_scatter_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t topk,
     if (slot < 0) return;
     const uint4 *src = a + (p / topk) * row_vecs;
     uint4 *dst = xg + (int64_t)slot * row_vecs;
-    for (int v0 = lane; v0 < row_vecs; v0 += 4 * 32) {  // four 16-byte loads in flight per lane
-        uint4 r[4];
+    // up to twelve 16-byte loads in flight per lane: a whole row of k = 2880 in one
+    // memory latency, which is what a decode-sized batch (few slots) waits for
+    for (int v0 = lane; v0 < row_vecs; v0 += kScatterVecs * 32) {
+        uint4 r[kScatterVecs];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < kScatterVecs; ++i)
             if (v0 + 32 * i < row_vecs) r[i] = __ldg(src + v0 + 32 * i);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < kScatterVecs; ++i)
             if (v0 + 32 * i < row_vecs) dst[v0 + 32 * i] = r[i];
     }
 }
 
-// One warp per token: 8 output columns (one 16-byte vector) per lane per step.
-// The token's slot rows and weights are read once; up to kCombineSlots slots all
-// vectors of a step are loaded before the sum, which still adds slot 0, 1, ... in
-// that order (a slot dropped by the scatter is skipped, not added as zero).
+// One warp per (token, chunk of chunk_vecs 16-byte vectors of its row): 8 output
+// columns (one vector) per lane per step. With many tokens a chunk is the whole row
+// (a warp per token); with few, the row is split so that enough warps are in flight
+// (each step's loads wait a memory latency). The token's slot rows and weights are
+// read by every warp of the token; up to kCombineSlots slots all vectors of a step
+// are loaded before the sum, which still adds slot 0, 1, ... in that order (a slot
+// dropped by the scatter is skipped, not added as zero).
 constexpr int kCombineSlots = 8;
 __device__ __forceinline__ void combine_add(float (&acc)[8], float w, const uint4 &q) {
     const uint32_t words[4] = {q.x, q.y, q.z, q.w};
@@ -150,12 +156,15 @@ __device__ __forceinline__ uint4 combine_pack(const float (&acc)[8]) {
 __global__ void __launch_bounds__(kThreads)
 moe_combine_kernel(const int32_t *__restrict__ pos, const float *__restrict__ weights,
                    int32_t topk, int64_t tokens, const uint4 *__restrict__ y, int32_t row_vecs,
-                   uint4 *__restrict__ out) {
-    const int64_t m = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+                   int32_t chunk_vecs, int32_t chunks, uint4 *__restrict__ out) {
+    const int64_t wid = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t m = wid / chunks;
     if (m >= tokens) return;
+    const int v0 = (int)(wid - m * chunks) * chunk_vecs;
+    const int v1 = v0 + chunk_vecs < row_vecs ? v0 + chunk_vecs : row_vecs;
     const int lane = threadIdx.x & 31;
     if (topk > kCombineSlots) {
-        for (int v = lane; v < row_vecs; v += 32) {
+        for (int v = v0 + lane; v < v1; v += 32) {
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             for (int j = 0; j < topk; ++j) {
                 const int32_t s = __ldg(pos + m * topk + j);
@@ -180,7 +189,7 @@ moe_combine_kernel(const int32_t *__restrict__ pos, const float *__restrict__ we
         w[j] = __shfl_sync(0xFFFFFFFFu, w_lane, j);
         rows[j] = (j < topk && s >= 0) ? y + (int64_t)s * row_vecs : nullptr;
     }
-    for (int v = lane; v < row_vecs; v += 32) {
+    for (int v = v0 + lane; v < v1; v += 32) {
         uint4 q[kCombineSlots];
 #pragma unroll
         for (int j = 0; j < kCombineSlots; ++j)
@@ -250,9 +259,22 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
     err = launch_mx_moe_gemm(act, offsets, experts, max_rows, pairs, w2_packed, w2_scales, k, n, y,
                              status, stream);
     if (err != cudaSuccess) return err;
-    moe_combine_kernel<<<(unsigned)((tokens + kWarps - 1) / kWarps), kThreads, 0, stream>>>(
+    // warps per token: enough to keep ~16 warps per SM in flight, at least 32 vectors
+    // (one per lane) per warp; a warp per token once tokens alone fill the GPU
+    int sms = 0, device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        sms = 0;
+    const int64_t want = (int64_t)(sms > 0 ? sms : 148) * 16;
+    const int32_t max_chunks = (k_vecs + 31) / 32;
+    int32_t chunks = (int32_t)((want + tokens - 1) / tokens);
+    chunks = chunks < 1 ? 1 : (chunks > max_chunks ? max_chunks : chunks);
+    const int32_t chunk_vecs = ((k_vecs + chunks - 1) / chunks + 31) / 32 * 32;
+    chunks = (k_vecs + chunk_vecs - 1) / chunk_vecs;
+    const int64_t combine_warps = tokens * chunks;
+    moe_combine_kernel<<<(unsigned)((combine_warps + kWarps - 1) / kWarps), kThreads, 0, stream>>>(
         pos, topk_weights, (int32_t)topk, tokens, reinterpret_cast<const uint4 *>(y), k_vecs,
-        reinterpret_cast<uint4 *>(out));
+        chunk_vecs, chunks, reinterpret_cast<uint4 *>(out));
     return cudaGetLastError();
 }
 
