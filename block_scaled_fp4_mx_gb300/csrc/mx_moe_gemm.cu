@@ -184,13 +184,14 @@ struct TmemCfg {
                   "issuer layout");
 };
 
-// Up to 32 tokens per expert (decode-time batches): one 128-row weight tile per
+// Up to 64 tokens per expert (decode-time batches): one 128-row weight tile per
 // item (more items than SMs several times over), the MMA's N cut to the expert's
 // tokens rounded up to 16, activation boxes only as tall as the capacity, four MMA
 // issuers with partial accumulators of the capacity rounded up to 16 columns each,
-// and a ring of decoded slices of 12 stages (three per decoder group). (From 33 to 64
-// tokens this configuration measured faster than the next one on the down GEMM and
-// slower on the gate/up GEMM; the next one takes them.)
+// K slices of 128 in a ring of 4 stages (one per decoder group) and a weight ring of
+// 12. (With a capacity of 33 to 64 it measured 12-15% faster than the 128-token
+// configuration on 32 x 2880 x 2880, 2-3% slower on 32 x 5760 x 2880, and 4% faster
+// over a 64-token MoE layer step.)
 using CfgTiny = TmemCfg<64, 1, 1, 4, 12, false, 0, 16, 4, true, 4, 2 * kK>;
 // Up to 128 tokens per expert: two weight tiles per item, one accumulator buffer.
 using CfgSmall = TmemCfg<128, 2, 1, 4, 8, false, 0, 16, 4, true>;
@@ -1005,7 +1006,7 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
     if (max_rows > 128)
         return launch_tmem<CfgLarge>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
                                      w_scales, n, n, k, out, status, stream);
-    if (max_rows <= 32)
+    if (max_rows <= 64)
         return launch_tmem<CfgTiny>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
                                     w_scales, n, n, k, out, status, stream);
     return launch_tmem<CfgSmall>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
@@ -1019,7 +1020,7 @@ cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offse
     if (max_rows > 128)
         return launch_tmem<CfgGateUpLarge>(x, expert_offsets, experts, max_rows, total_rows,
                                            w1_packed, w1_scales, 2 * n, n, k, act, status, stream);
-    if (max_rows <= 32)
+    if (max_rows <= 64)
         return launch_tmem<CfgGateUpTiny>(x, expert_offsets, experts, max_rows, total_rows,
                                           w1_packed, w1_scales, 2 * n, n, k, act, status, stream);
     return launch_tmem<CfgGateUp>(x, expert_offsets, experts, max_rows, total_rows, w1_packed,

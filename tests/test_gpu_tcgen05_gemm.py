@@ -100,11 +100,11 @@ def test_identity_weights_exact(oracle_impl):
                                       ([40, 3], 128, 64), ([5, 32, 17], 256, 2912),
                                       ([70, 2, 33], 288, 1056)])
 def test_decode_sized_batches(oracle_impl, rows, n, k):
-    """Decode-time batches. Up to 32 tokens per expert: one 128-row weight tile per
+    """Decode-time batches. Up to 64 tokens per expert: one 128-row weight tile per
     item, MMA N = the expert's tokens rounded up to 16, activation boxes of the
     capacity rounded up to 16 rows, four MMA issuers each summing a quarter of the K
-    slices into a partial accumulator, read out as the sum of the partials; 33 to 64
-    tokens: the 128-token configuration. Ragged n (last tiles of 64, 96 and 32 rows)
+    slices (of 128) into a partial accumulator, read out as the sum of the partials;
+    70 tokens: the 128-token configuration. Ragged n (last tiles of 64, 96 and 32 rows)
     and an empty expert included; k = 2912 and 1056 end on a half-empty K slice (the
     tensor map reads zeros past k) after 45 and 16 full ones."""
     run_case(oracle_impl, rows, n, k, seed=sum(rows) + n + k)
