@@ -60,21 +60,29 @@ moe_route_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t experts
             atomicAdd(counts + e, 1);
     }
     __syncthreads();
-    if (local)
-        for (int e = t; e < experts; e += kThreads)
-            if (hist[e] != 0) atomicAdd(counts + e, hist[e]);
-    __threadfence();  // this block's counts are visible before its ticket
-    __syncthreads();
-    if (t == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
+    // one block (a decode-sized batch): its shared histogram is the whole count, so it
+    // stores the counts and scans them itself, with no global atomics, fence or ticket
+    const bool single = gridDim.x == 1 && local;
+    if (single) {
+        for (int e = t; e < experts; e += kThreads) counts[e] = hist[e];
+    } else {
+        if (local)
+            for (int e = t; e < experts; e += kThreads)
+                if (hist[e] != 0) atomicAdd(counts + e, hist[e]);
+        __threadfence();  // this block's counts are visible before its ticket
+        __syncthreads();
+        if (t == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+    }
     // thread t sums a contiguous run of experts, the block scans the run sums
     const int per = (experts + kThreads - 1) / kThreads;
     const int e0 = t * per;
     const int e1 = e0 + per < experts ? e0 + per : experts;
+    auto count_of = [&](int e) -> int32_t { return single ? hist[e] : __ldcg(counts + e); };
     int64_t sum = 0;
-    for (int e = e0; e < e1; ++e) sum += __ldcg(counts + e);
+    for (int e = e0; e < e1; ++e) sum += count_of(e);
     part[t] = sum;
     __syncthreads();
     for (int d = 1; d < kThreads; d <<= 1) {  // inclusive Hillis-Steele scan
@@ -85,7 +93,7 @@ moe_route_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t experts
     }
     int64_t run = part[t] - sum;  // exclusive prefix of this thread's run
     for (int e = e0; e < e1; ++e) {
-        const int32_t c = __ldcg(counts + e);
+        const int32_t c = count_of(e);
         offsets[e] = run;
         cursors[e] = (int32_t)run;
         if (c > max_rows) atomicExch(status, FP4_ERR_SHAPE);
@@ -238,10 +246,15 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
     uint16_t *act = reinterpret_cast<uint16_t *>(ws + L.act);
     uint16_t *y = reinterpret_cast<uint16_t *>(ws + L.y);
     const int64_t pairs = tokens * topk;
-    cudaError_t err = cudaMemsetAsync(counts, 0, (size_t)(experts + 1) * 4, stream);  // + ticket
-    if (err != cudaSuccess) return err;
+    const int64_t blocks = (pairs + kThreads - 1) / kThreads;
+    cudaError_t err = cudaSuccess;
+    // the counters and the ticket start at zero when several blocks add into them; a
+    // single block (a decode-sized batch) stores its counts and takes no ticket
+    if (blocks > 1 || experts > kLocalExperts) {
+        err = cudaMemsetAsync(counts, 0, (size_t)(experts + 1) * 4, stream);  // + ticket
+        if (err != cudaSuccess) return err;
+    }
     {
-        const int64_t blocks = (pairs + kThreads - 1) / kThreads;
         const int grid = (int)(blocks < 1024 ? blocks : 1024);
         const size_t hist_bytes = experts <= kLocalExperts ? (size_t)experts * 4 : 0;
         moe_route_kernel<<<grid, kThreads, hist_bytes, stream>>>(
