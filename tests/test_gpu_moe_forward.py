@@ -209,10 +209,13 @@ def test_extended_last_slabs(oracle_impl):
     check(oracle_impl, L)
 
 
-def test_many_experts(oracle_impl):
+@pytest.mark.parametrize("tokens,experts", [(64, 5000), (64, 600), (128, 4096), (129, 300)])
+def test_many_experts(oracle_impl, tokens, experts):
     """5000 experts: more than the route kernel's shared-memory histogram holds
-    (global atomics) and more than the GEMMs' compact item list (dense list)."""
-    check(oracle_impl, make_layer(64, 32, 32, 5000, 2, seed=57))
+    (global atomics) and more than the GEMMs' compact item list (dense list). 600 and
+    4096 experts with at most 256 slots: one route block scans its own histogram,
+    several experts per thread; 129 tokens: 258 slots, two route blocks."""
+    check(oracle_impl, make_layer(tokens, 32, 32, experts, 2, seed=57 + experts))
 
 
 def test_full_size_layer_sampled_tokens(oracle_impl):
