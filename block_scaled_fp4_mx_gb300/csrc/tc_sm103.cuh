@@ -118,6 +118,42 @@ __device__ __forceinline__ uint32_t mma_slice_tmem_a(uint32_t d_tmem, uint32_t a
     return ready;
 }
 
+// mma_slice_tmem_a over two 64-wide K sub-slices: eight K = 16 steps, A advancing 8
+// columns per step across both, B taking each sub-slice's four steps from its own
+// descriptor (b_desc, b2_desc); the same probe of the next stage's barrier and one
+// commit to `empty_bar`.
+__device__ __forceinline__ uint32_t mma_slice2_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                      uint64_t b2_desc, uint32_t idesc,
+                                                      uint32_t accumulate, uint32_t empty_bar,
+                                                      uint32_t next_bar, uint32_t next_phase) {
+    uint32_t ready;
+    asm volatile(
+        "{\n\t.reg .pred pr, p0, pt;\n\t.reg .b64 b1, b2, b3, c1, c2, c3;\n\t"
+        ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pr, [%8], %9;\n\t"
+        "setp.ne.b32 p0, %6, 0;\n\tsetp.eq.b32 pt, %6, %6;\n\t"
+        "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+        "add.u64 c1, %4, 2;\n\tadd.u64 c2, %4, 4;\n\tadd.u64 c3, %4, 6;\n\t"
+        "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
+        "add.u32 a4, %2, 32;\n\tadd.u32 a5, %2, 40;\n\tadd.u32 a6, %2, 48;\n\t"
+        "add.u32 a7, %2, 56;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %5, p0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a4], %4, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a5], c1, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a6], c2, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a7], c3, %5, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+        "selp.u32 %0, 1, 0, pr;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "l"(b2_desc), "r"(idesc), "r"(accumulate),
+          "r"(empty_bar), "r"(next_bar), "r"(next_phase)
+        : "memory");
+    return ready;
+}
+
 // One K slice of MMAs with A in tensor memory (four K = 16 steps: A advances 8
 // columns and the B descriptor 32 bytes per step) and a commit to `empty_bar`.
 // `accumulate` = 0 overwrites D with the first step.
