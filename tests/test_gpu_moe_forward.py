@@ -157,12 +157,13 @@ def test_pages_zero_code_layer_is_exactly_zero():
 @pytest.mark.parametrize("tokens,k,n,experts,topk", [(1, 32, 32, 1, 1), (40, 128, 96, 5, 2),
                                                      (37, 64, 160, 3, 3), (130, 96, 64, 4, 1),
                                                      (300, 128, 96, 3, 2), (700, 64, 224, 2, 1),
-                                                     (400, 32, 32, 2, 1)])
+                                                     (400, 32, 32, 2, 1), (100, 192, 96, 4, 2)])
 def test_small_layers(oracle_impl, tokens, k, n, experts, topk):
     """Single token and expert; n and k that are not multiples of the tiles; more
     than 128 tokens (256-token slabs: gate and up halves in one tile, N = 128 MMAs
     for slabs with at most 128 live tokens, ragged 64-column tiles, and n = 32: half
-    of one 64-column tile); topk 1 to 3."""
+    of one 64-column tile); a capacity of 100 (gate and up tiles of 128 rows, K slices
+    of 128 ending half-empty); topk 1 to 3."""
     check(oracle_impl, make_layer(tokens, k, n, experts, topk, seed=tokens + k + n))
 
 
@@ -249,6 +250,12 @@ def test_decode_step_layer(oracle_impl):
 def test_gpt_oss_like_layer(oracle_impl):
     """Hidden 2880, intermediate 2880, 4 experts, top-4 of 64 tokens."""
     check(oracle_impl, make_layer(64, 2880, 2880, 4, 4, seed=31))
+
+
+def test_gpt_oss_like_layer_128_tokens(oracle_impl):
+    """Hidden 2880, intermediate 2880, 4 experts, top-4 of 128 tokens: the gate/up
+    GEMM with gate and up tiles of 128 rows and the down GEMM's two-tile items."""
+    check(oracle_impl, make_layer(128, 2880, 2880, 4, 4, seed=37))
 
 
 def test_gpt_oss_like_layer_normal_activations(oracle_impl):
