@@ -12,11 +12,12 @@
 // can be the tensor core's A operand, which tcgen05.mma reads from tensor memory:
 //     D[weight row][token] = sum_k W[weight row][k] * X[token][k],
 // 128 weight rows per M tile (one per TMEM lane), the expert's tokens as N. A
-// decoder thread owns one weight row of a 64-wide K slice: it decodes the row's
-// 64 codes (two E8M0 blocks) in registers and writes them with one tcgen05.st
-// into its own TMEM lane, 32 columns of bf16 pairs. There is no shared-memory
-// copy of the decoded tile, no generic-to-async proxy fence, and the ring of
-// decoded slices can be deep because tensor memory is otherwise idle.
+// decoder thread owns one weight row of a K slice (64 wide, or 128 = two 64-wide
+// sub-slices in the configurations for up to 128 tokens): it decodes the row's 64
+// codes of a sub-slice (two E8M0 blocks) in registers and writes them with one
+// tcgen05.st into its own TMEM lane, 32 columns of bf16 pairs. There is no
+// shared-memory copy of the decoded tile, no generic-to-async proxy fence, and the
+// ring of decoded slices can be deep because tensor memory is otherwise idle.
 //
 // One CTA per SM walks a static list of work items (expert, token slab, tile of
 // weight rows; consecutive items share the expert's activation rows in L2). With
@@ -24,14 +25,15 @@
 // step then issues a second MMA (N = 16..64) on the same decoded weights into
 // accumulator columns 256.., so an expert of 257..320 rows (or 513..576, ...)
 // needs no extra item and no extra decode of its weights. A
-// stage of the operand ring holds one 64-wide K slice: its activation tile in
-// shared memory and its decoded weights in tensor memory, under one "full"
-// barrier (the TMA bytes plus one arrival per decoder warp) and one "empty"
-// barrier (the MMA commit):
-//   - one TMA thread streams the activation tiles (kTok tokens x 64 bf16,
-//     128-byte swizzle, the MMA's B operand);
-//   - another streams the packed codes of the weight slices (rows x 32 bytes of
-//     a 2-D uint8 tensor map) through a ring of its own;
+// stage of the operand ring holds one K slice: its activation tile(s) in shared
+// memory and its decoded weights in tensor memory, under one "full" barrier (the
+// TMA bytes plus one arrival per decoder warp) and one "empty" barrier (the MMA
+// commit):
+//   - one TMA thread streams the activation tiles (kTok tokens x 64 bf16 per
+//     sub-slice, 128-byte swizzle, the MMA's B operand);
+//   - another streams the packed codes of the weight slices (rows x 32 bytes, or
+//     x 64 bytes with the 64-byte swizzle for slices of 128, of a 2-D uint8 tensor
+//     map) through a ring of its own;
 //   - 16 decoder warps: warp w writes TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31,
 //     so 4 warps cover one 128-row M tile; the kMTw tiles of a slice take 4 kMTw
 //     warps and the remaining warps form further groups that own every kGroups-th
