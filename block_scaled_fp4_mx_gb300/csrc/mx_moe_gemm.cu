@@ -7,8 +7,11 @@
 // weights to bf16 and multiplies it with bf16 activations. Here the bf16 weights
 // never reach HBM (0.53 bytes per weight are read instead of 2 + 2 for unpack,
 // store and reload) and never touch shared memory either: bf16 activations x
-// MXFP4 weights decoded exactly as fp4_mx_unpack decodes them, fp32 accumulation
-// in tensor memory, bf16 out. The operands are swapped so that the decoded weights
+// MXFP4 weights decoded to the values fp4_mx_unpack gives them, fp32 accumulation
+// in tensor memory, bf16 out. (A zero code with the sign bit set stays -0.0 here:
+// as a factor it adds nothing to a sum either way, and skipping the +0.0 fix saves
+// two of the decode's ~15 integer operations per 8 codes, 5-8% of the decode-time
+// GEMM's time on GB300.) The operands are swapped so that the decoded weights
 // can be the tensor core's A operand, which tcgen05.mma reads from tensor memory:
 //     D[weight row][token] = sum_k W[weight row][k] * X[token][k],
 // 128 weight rows per M tile (one per TMEM lane), the expert's tokens as N. A
@@ -181,7 +184,12 @@ struct TmemCfg {
                   "tensor memory columns");
     static_assert(kSmemBytes <= 232448, "shared memory per block");
     // several issuers: four (one per decoder group and epilogue warp), one weight tile,
-    // one accumulator buffer, ring stages in whole rounds of the four groups
+    // one accumulator buffer, ring stages in whole rounds of the four groups. The last
+    // is what keeps the parity waits sound: stage s is then used by one decoder group
+    // and one issuer only, so nobody reaches use u of a stage before use u - 1 is under
+    // way. With another ring length a stage's uses pass between groups, a fast waiter
+    // can be a whole use ahead, and a parity wait cannot tell phase u from u - 2 (a
+    // 7-stage ring faulted on GB300 that way).
     static_assert(kIssuers == 1 || (kIssuers == 4 && kGroups == 4 && kEpiWarps == 4 && kMTw == 1 &&
                                     kAccBufs == 1 && kExt == 0 && S % 4 == 0 && kEpiWarp0 % 4 == 0),
                   "issuer layout");
@@ -472,7 +480,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const uint4 v = mx_decode_word(words[q], q < 4 ? t0 : t1);
+                    const uint4 v = mx_decode_word_operand(words[q], q < 4 ? t0 : t1);
                     d[4 * q + 0] = v.x;
                     d[4 * q + 1] = v.y;
                     d[4 * q + 2] = v.z;
@@ -501,7 +509,7 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     const uint32_t words2[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const uint4 v = mx_decode_word(words2[q], q < 4 ? t2 : t3);
+                        const uint4 v = mx_decode_word_operand(words2[q], q < 4 ? t2 : t3);
                         d[4 * q + 0] = v.x;
                         d[4 * q + 1] = v.y;
                         d[4 * q + 2] = v.z;
