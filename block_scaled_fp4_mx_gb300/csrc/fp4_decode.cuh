@@ -98,16 +98,6 @@ __device__ __forceinline__ uint4 mx_decode_word(uint32_t w, const ByteTable &t) 
     return lookup_word(w, t, negative_nonzero);
 }
 
-// MXFP4 decode of one word for use as a matrix operand only: every code takes its
-// sign, so code 8 comes out as -0.0 instead of +0.0. A product with -0.0 is a zero
-// like one with +0.0 and adds nothing to a sum, so a dot product over these values
-// equals the one over the exact decode (only an all-zero sum may differ in the sign
-// of its zero). Two integer operations fewer per word than mx_decode_word (lookup_word
-// keeps only bit 3 of each sign nibble).
-__device__ __forceinline__ uint4 mx_decode_word_operand(uint32_t w, const ByteTable &t) {
-    return lookup_word(w, t, w);
-}
-
 // MXFP4 decode of one code, written independently of the table path (used by
 // the kernel for unaligned buffers).
 __device__ __forceinline__ uint16_t mx_decode_code(uint32_t code, uint32_t e8m0) {

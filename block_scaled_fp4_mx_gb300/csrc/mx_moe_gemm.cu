@@ -220,6 +220,16 @@ using CfgGateUpTiny = TmemCfg<64, 1, 1, 4, 12, true, 0, 16, 4, true, 4, 2 * kK>;
 // weight tile.
 using CfgGateUpLarge = TmemCfg<256, 1, 1, 5, 5, true, 64, 12, 8>;
 
+// MXFP4 decode of one word for use as a matrix operand only: every code takes its
+// sign, so code 8 comes out as -0.0 instead of +0.0. A product with -0.0 is a zero
+// like one with +0.0 and adds nothing to a sum, so a dot product over these values
+// equals the one over the exact decode (only an all-zero sum may differ in the sign
+// of its zero). Two integer operations fewer per word than mx_decode_word (lookup_word
+// keeps only bit 3 of each sign nibble).
+__device__ __forceinline__ uint4 mx_decode_word_operand(uint32_t w, const ByteTable &t) {
+    return lookup_word(w, t, w);
+}
+
 struct Item {
     int64_t row_begin, rows, m0;
     int expert, n0;
