@@ -4,10 +4,36 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
 namespace fp4mx {
+
+// Launch `kernel`; with `after_kernel` it may start while the kernel before it in the
+// stream is still finishing (programmatic dependent launch): it must then wait
+// (grid_dependency_wait) before it touches anything that kernel writes or reads.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool after_kernel, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_kernel ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// In a kernel launched with after_kernel: returns once the kernel before it in the
+// stream has completed and its memory operations are visible (at once otherwise).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // Decode n_elems (a positive multiple of 32) MXFP4 codes.
 cudaError_t launch_mx_unpack(const uint8_t *packed, const uint8_t *scales, uint16_t *out,
@@ -30,10 +56,13 @@ cudaError_t launch_mx_quantize(const uint16_t *in, uint8_t *packed, uint8_t *sca
 
 // Grouped MoE GEMM with MXFP4 weights decoded into the tensor-core A operand in
 // tensor memory (any shape the entry point accepts; 16-byte aligned weights).
+// With after_kernel (inside the MoE layer) it may start while the kernel before it
+// finishes: only its activation loads wait for that kernel, so the activations must
+// be that kernel's output or older, and everything else it reads must be older.
 cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets, int64_t experts,
                                int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
                                const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
-                               int32_t *status, cudaStream_t stream);
+                               int32_t *status, cudaStream_t stream, bool after_kernel = false);
 
 // The MoE layer's gate/up GEMM: x [total_rows, k] against w1 [experts, 2n, k/2]
 // (gate rows 0..n-1, up rows n..2n-1 of each expert) -> act [total_rows, n] =
@@ -41,7 +70,7 @@ cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets,
 cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offsets, int64_t experts,
                                   int64_t max_rows, int64_t total_rows, const uint8_t *w1_packed,
                                   const uint8_t *w1_scales, int64_t n, int64_t k, uint16_t *act,
-                                  int32_t *status, cudaStream_t stream);
+                                  int32_t *status, cudaStream_t stream, bool after_kernel = false);
 
 // The MoE layer: routing, gate/up GEMM with silu(gate) * up, down GEMM, top-k
 // weighted sum. Byte offsets of its scratch arrays in the caller's workspace.

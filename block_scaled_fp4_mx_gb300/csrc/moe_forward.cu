@@ -109,6 +109,7 @@ moe_scatter_kernel(const int32_t *__restrict__ ids, int64_t pairs, int32_t topk,
                    int64_t max_rows, const int32_t *__restrict__ counts,
                    const uint4 *__restrict__ a, int32_t row_vecs, int32_t *__restrict__ cursors,
                    int32_t *__restrict__ pos, uint4 *__restrict__ xg) {
+    grid_dependency_wait();  // the route kernel's counts and cursors
     const int64_t p = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (p >= pairs) return;
     const int lane = threadIdx.x & 31;
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kThreads)
 moe_combine_kernel(const int32_t *__restrict__ pos, const float *__restrict__ weights,
                    int32_t topk, int64_t tokens, const uint4 *__restrict__ y, int32_t row_vecs,
                    int32_t chunk_vecs, int32_t chunks, uint4 *__restrict__ out) {
+    grid_dependency_wait();  // the down GEMM's rows
     const int64_t wid = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int64_t m = wid / chunks;
     if (m >= tokens) return;
@@ -260,17 +262,25 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
         moe_route_kernel<<<grid, kThreads, hist_bytes, stream>>>(
             topk_ids, pairs, (int32_t)experts, max_rows, counts, ticket, offsets, cursors, status);
     }
-    const int32_t k_vecs = (int32_t)(k / 8);
-    moe_scatter_kernel<<<(unsigned)((pairs + kWarps - 1) / kWarps), kThreads, 0, stream>>>(
-        topk_ids, pairs, (int32_t)topk, (int32_t)experts, max_rows, counts,
-        reinterpret_cast<const uint4 *>(a), k_vecs, cursors, pos, reinterpret_cast<uint4 *>(xg));
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    // The kernels after the route kernel start while the one before them finishes
+    // (programmatic dependent launch) and wait for it where they read its output:
+    // scatter and combine on entry, the GEMMs in their activation loads. Everything
+    // else they read is older than the route kernel, which starts only after all
+    // earlier work in the stream, and so are the last readers of what they write.
+    const int32_t k_vecs = (int32_t)(k / 8);
+    err = launch_kernel(moe_scatter_kernel, dim3((unsigned)((pairs + kWarps - 1) / kWarps)),
+                        dim3(kThreads), 0, stream, true, topk_ids, pairs, (int32_t)topk,
+                        (int32_t)experts, max_rows, (const int32_t *)counts,
+                        reinterpret_cast<const uint4 *>(a), k_vecs, cursors, pos,
+                        reinterpret_cast<uint4 *>(xg));
+    if (err != cudaSuccess) return err;
     err = launch_mx_moe_gate_up(xg, offsets, experts, max_rows, pairs, w1_packed, w1_scales, n, k,
-                                act, status, stream);
+                                act, status, stream, true);
     if (err != cudaSuccess) return err;
     err = launch_mx_moe_gemm(act, offsets, experts, max_rows, pairs, w2_packed, w2_scales, k, n, y,
-                             status, stream);
+                             status, stream, true);
     if (err != cudaSuccess) return err;
     // warps per token: enough to keep ~16 warps per SM in flight, at least 32 vectors
     // (one per lane) per warp; a warp per token once tokens alone fill the GPU
@@ -285,10 +295,10 @@ cudaError_t launch_mx_moe_forward(const uint16_t *a, const int32_t *topk_ids,
     const int32_t chunk_vecs = ((k_vecs + chunks - 1) / chunks + 31) / 32 * 32;
     chunks = (k_vecs + chunk_vecs - 1) / chunk_vecs;
     const int64_t combine_warps = tokens * chunks;
-    moe_combine_kernel<<<(unsigned)((combine_warps + kWarps - 1) / kWarps), kThreads, 0, stream>>>(
-        pos, topk_weights, (int32_t)topk, tokens, reinterpret_cast<const uint4 *>(y), k_vecs,
-        chunk_vecs, chunks, reinterpret_cast<uint4 *>(out));
-    return cudaGetLastError();
+    return launch_kernel(moe_combine_kernel, dim3((unsigned)((combine_warps + kWarps - 1) / kWarps)),
+                         dim3(kThreads), 0, stream, true, (const int32_t *)pos, topk_weights,
+                         (int32_t)topk, tokens, reinterpret_cast<const uint4 *>(y), k_vecs,
+                         chunk_vecs, chunks, reinterpret_cast<uint4 *>(out));
 }
 
 }  // namespace fp4mx

@@ -764,6 +764,9 @@ mx_moe_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         }
     } else if (warp == C::kTmaXWarp && lane == 0) {
         // ---- TMA: activation tiles ----
+        // launched behind the kernel that writes the activations (the MoE layer), the
+        // kernel may start while that one finishes: the activation loads wait for it
+        grid_dependency_wait();
         int s = 0;
         uint32_t ph = 0, g = 0;
         bool stop = false;
@@ -999,7 +1002,7 @@ template <class C>
 cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_t experts,
                         int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
                         const uint8_t *w_scales, int64_t n_rows, int64_t n_out, int64_t k,
-                        uint16_t *out, int32_t *status, cudaStream_t stream) {
+                        uint16_t *out, int32_t *status, cudaStream_t stream, bool after_kernel) {
     static thread_local int configured_device = -1;
     int device = 0;
     cudaError_t err = cudaGetDevice(&device);
@@ -1023,10 +1026,10 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(items < sms ? items : sms);
-    mx_moe_gemm_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-        map_x, map_x_ext, map_w, expert_offsets, w_scales, (int32_t)experts, max_rows, total_rows,
-        (int32_t)n_rows, (int32_t)n_out, (int32_t)k, (int32_t)x_box_rows, out, status);
-    return cudaGetLastError();
+    return launch_kernel(mx_moe_gemm_kernel<C>, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
+                         stream, after_kernel, map_x, map_x_ext, map_w, expert_offsets, w_scales,
+                         (int32_t)experts, max_rows, total_rows, (int32_t)n_rows, (int32_t)n_out,
+                         (int32_t)k, (int32_t)x_box_rows, out, status);
 }
 
 }  // namespace
@@ -1034,29 +1037,31 @@ cudaError_t launch_tmem(const uint16_t *a, const int64_t *expert_offsets, int64_
 cudaError_t launch_mx_moe_gemm(const uint16_t *a, const int64_t *expert_offsets, int64_t experts,
                                int64_t max_rows, int64_t total_rows, const uint8_t *w_packed,
                                const uint8_t *w_scales, int64_t n, int64_t k, uint16_t *out,
-                               int32_t *status, cudaStream_t stream) {
+                               int32_t *status, cudaStream_t stream, bool after_kernel) {
     if (max_rows > 128)
         return launch_tmem<CfgLarge>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
-                                     w_scales, n, n, k, out, status, stream);
+                                     w_scales, n, n, k, out, status, stream, after_kernel);
     if (max_rows <= 64)
         return launch_tmem<CfgTiny>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
-                                    w_scales, n, n, k, out, status, stream);
+                                    w_scales, n, n, k, out, status, stream, after_kernel);
     return launch_tmem<CfgSmall>(a, expert_offsets, experts, max_rows, total_rows, w_packed,
-                                 w_scales, n, n, k, out, status, stream);
+                                 w_scales, n, n, k, out, status, stream, after_kernel);
 }
 
 cudaError_t launch_mx_moe_gate_up(const uint16_t *x, const int64_t *expert_offsets, int64_t experts,
                                   int64_t max_rows, int64_t total_rows, const uint8_t *w1_packed,
                                   const uint8_t *w1_scales, int64_t n, int64_t k, uint16_t *act,
-                                  int32_t *status, cudaStream_t stream) {
+                                  int32_t *status, cudaStream_t stream, bool after_kernel) {
     if (max_rows > 128)
         return launch_tmem<CfgGateUpLarge>(x, expert_offsets, experts, max_rows, total_rows,
-                                           w1_packed, w1_scales, 2 * n, n, k, act, status, stream);
+                                           w1_packed, w1_scales, 2 * n, n, k, act, status, stream,
+                                           after_kernel);
     if (max_rows <= 64)
         return launch_tmem<CfgGateUpTiny>(x, expert_offsets, experts, max_rows, total_rows,
-                                          w1_packed, w1_scales, 2 * n, n, k, act, status, stream);
+                                          w1_packed, w1_scales, 2 * n, n, k, act, status, stream,
+                                          after_kernel);
     return launch_tmem<CfgGateUp>(x, expert_offsets, experts, max_rows, total_rows, w1_packed,
-                                  w1_scales, 2 * n, n, k, act, status, stream);
+                                  w1_scales, 2 * n, n, k, act, status, stream, after_kernel);
 }
 
 }  // namespace fp4mx
