@@ -377,6 +377,44 @@ def test_graph_capture_and_replay(oracle_impl):
         assert (np.abs(got - r["out"]) <= tol).all()
 
 
+@pytest.mark.parametrize("tokens,topk", [(40, 2), (300, 2)])
+def test_back_to_back_calls_on_inputs_written_just_before(oracle_impl, tokens, topk):
+    """Four layer calls in a row on one stream, with no host synchronisation between
+    them: before each call, device copies on the same stream overwrite every input
+    (activations, routing, top-k weights and all four weight tensors) in the same
+    buffers, and the call reuses one workspace and one output, whose copy is taken
+    right after it. The kernels after the routing kernel start while their
+    predecessor finishes; each result must still match the oracle for its own
+    inputs. 40 tokens: the decode-time GEMMs; 300: 256-token slabs."""
+    k, n, experts = 128, 96, 4
+    layers = [make_layer(tokens, k, n, experts, topk, seed=500 + i) for i in range(4)]
+    keys = ("ids", "wts", "w1p", "w1s", "w2p", "w2s")
+    src = [dict({key: torch.from_numpy(L[key]).to(DEV) for key in keys},
+                a=torch.from_numpy(L["a_bits"].view(np.int16)).to(DEV).view(torch.bfloat16))
+           for L in layers]
+    buf = {key: torch.empty_like(src[0][key]) for key in keys + ("a",)}
+    ws = torch.empty(fp4.fp4_mx_moe_workspace_bytes(tokens, topk, experts, n, k), dtype=torch.uint8,
+                     device=DEV)
+    out = torch.empty(tokens, k, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    results = []
+    for s in src:
+        for key in buf:
+            buf[key].copy_(s[key])
+        fp4.fp4_mx_moe_forward(buf["a"], buf["ids"], buf["wts"], buf["w1p"], buf["w1s"], buf["w2p"],
+                               buf["w2s"], out=out, workspace=ws, status=status)
+        results.append(out.clone())
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for L, res in zip(layers, results):
+        got = res.float().cpu().numpy().astype(np.float64)
+        r = oracle_impl.mx_moe_forward(L["a_bits"], L["ids"], L["wts"], L["w1p"], L["w1s"], L["w2p"],
+                                       L["w2s"], threads=oracle_impl.max_threads())
+        tol = forward_bound(r, L["ids"], L["wts"], k, n, topk, exact_gemm1=True)
+        assert (np.abs(got - r["out"]) <= tol).all()
+
+
 def test_concurrent_host_threads(oracle_impl):
     """Four host threads, each on its own CUDA stream, call the MXFP4 unpack, the
     NVFP4 gather and the layer ten times each into outputs of their own: every result
