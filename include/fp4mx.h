@@ -3,7 +3,8 @@
  * (E2M1) data into bf16.
  *
  * The operations below; each is one CUDA kernel launch on the caller's stream,
- * except the MoE layer (one memset and five launches):
+ * except the MoE layer (one memset and five launches, the last four of which may
+ * start while the one before them finishes):
  *
  *   fp4_mx_unpack             MXFP4: one E8M0 scale byte per 32 codes, applied as
  *                             a wrapping 16-bit integer add into the bf16 exponent
@@ -199,6 +200,8 @@ fp4_status fp4_mx_quantize(const uint16_t *in_bf16, uint8_t *packed_out, uint8_t
  * where W_e[j][k] is the bf16 value fp4_mx_unpack gives for row j of expert e's
  * packed weights. Products and sums are accumulated in fp32 by the tensor core
  * (summation order unspecified), then rounded to bf16 (nearest, ties to even).
+ * (The zero code with the sign bit set enters the products as -0.0 rather than
+ * +0.0: the same value, so only the sign of an all-zero sum can differ.)
  *
  *   a_bf16               device, uint16[total_rows * k] bf16 bits, row-major, the rows
  *                        of each expert contiguous; 16-byte aligned
@@ -244,8 +247,9 @@ fp4_status fp4_mx_moe_gemm(const uint16_t *a_bf16, const int64_t *expert_offsets
  *     act = bf16(silu(h[:n]) * h[n:])   silu(x) = x / (1 + exp(-x)), fp32
  *     y   = bf16(act @ W2_e^T)          W2_e [k, n]
  *     out[m] = bf16(sum_j w * y)        fp32, slots in order j = 0, 1, ...
- * where W1_e and W2_e are what fp4_mx_unpack gives for the expert's packed rows,
- * and the GEMMs accumulate in fp32 on the tensor core (order unspecified).
+ * where W1_e and W2_e are what fp4_mx_unpack gives for the expert's packed rows
+ * (as values: a zero code may enter a product as -0.0), and the GEMMs accumulate
+ * in fp32 on the tensor core (order unspecified).
  *
  *   a_bf16               device, uint16[tokens * k] bf16 bits, row-major; 16-byte aligned
  *   topk_ids             device, int32[tokens * topk]; an id outside [0, experts)
