@@ -56,6 +56,41 @@ def run_case(ref, rows, n, k, seed, e_lo=118, e_hi=132, max_rows=None, a_scale=1
     return got, exact
 
 
+@pytest.mark.parametrize("rows,n,k", [([8, 8, 3, 8], 256, 576), ([100, 70, 100], 256, 576),
+                                      ([300, 40], 128, 320)])
+def test_negative_zero_codes_equal_positive_zero(rows, n, k):
+    """The GEMM's decode lets the zero code with the sign bit set (code 8) through as
+    -0.0, where fp4_mx_unpack gives +0.0. As a factor it is the same value: with every
+    code 0 of random weights turned into code 8, every output is the same value, and
+    bit for bit the same wherever it is not zero (decode-time, 128-token and 256-token
+    configurations). Weights of code 8 alone give zeros."""
+    experts = len(rows)
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    total = int(offsets[-1])
+    rng = np.random.default_rng(4242)
+    a_bits = inputs.bf16_normal_bits(rng, total * k).reshape(total, k)
+    w = inputs.mx_random(experts * n, k, 4243, e_lo=118, e_hi=132, zero_fraction=True)
+    packed = w.packed.reshape(experts, n, k // 2)
+    lo, hi = packed & 0x0F, packed >> 4
+    flipped = (np.where(lo == 0, 8, lo) | (np.where(hi == 0, 8, hi) << 4)).astype(np.uint8)
+    assert (lo == 0).any() and (hi == 0).any()
+    a_t = torch.from_numpy(a_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    off_t = torch.from_numpy(offsets).to(DEV)
+    s_t = torch.from_numpy(w.scales.reshape(experts, n, k // 32)).to(DEV)
+    outs = []
+    for pk in (packed, flipped, np.full_like(packed, 0x88)):
+        out, status = fp4.fp4_mx_moe_gemm(a_t, off_t, torch.from_numpy(pk).to(DEV), s_t, max(rows))
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append(out)
+    plus, minus, zero = (o.float().cpu().numpy() for o in outs)
+    assert np.array_equal(plus, minus)  # as values (-0.0 == +0.0)
+    nz = plus != 0
+    bits = [o.view(torch.int16).cpu().numpy() for o in outs[:2]]
+    assert np.array_equal(bits[0][nz], bits[1][nz])
+    assert (zero == 0).all()
+
+
 def test_single_tile(oracle_impl):
     """One expert, one 128 x 128 tile, one 64-wide K slice (four MMAs)."""
     run_case(oracle_impl, [128], 128, 64, seed=1)
