@@ -91,6 +91,15 @@ def test_negative_zero_codes_equal_positive_zero(rows, n, k):
     assert (zero == 0).all()
 
 
+@pytest.mark.parametrize("rows,n,k", [([5, 0, 3], 160, 32), ([5, 9], 96, 96), ([100, 70], 256, 32),
+                                      ([128, 1], 128, 96), ([300], 128, 32), ([257, 3], 96, 96)])
+def test_single_partial_k_slice(oracle_impl, rows, n, k):
+    """k of 32 or 96: one K slice of 128 (or of 64 with 256-token slabs), mostly past k
+    (the tensor maps read zeros there), in each configuration: decode-time (up to 64
+    tokens), 128-token and 256-token."""
+    run_case(oracle_impl, rows, n, k, seed=sum(rows) + 7 * n + k)
+
+
 def test_single_tile(oracle_impl):
     """One expert, one 128 x 128 tile, one 64-wide K slice (four MMAs)."""
     run_case(oracle_impl, [128], 128, 64, seed=1)
