@@ -33,7 +33,9 @@
 // TMA bytes plus one arrival per decoder warp) and one "empty" barrier (the MMA
 // commit):
 //   - one TMA thread streams the activation tiles (kTok tokens x 64 bf16 per
-//     sub-slice, 128-byte swizzle, the MMA's B operand);
+//     sub-slice, 128-byte swizzle, the MMA's B operand); inside the MoE layer the
+//     kernel is a dependent launch that may start while the kernel writing the
+//     activations finishes, and this thread alone waits for that kernel;
 //   - another streams the packed codes of the weight slices (rows x 32 bytes, or
 //     x 64 bytes with the 64-byte swizzle for slices of 128, of a 2-D uint8 tensor
 //     map) through a ring of its own;
